@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Decode-step throughput of the GB300 HiSparse hot path; prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ctx128k] [--impl reference]
+
+A step is one pass of the whole hot path over one decode batch: append the new
+rows, then per indexer group indexer scoring + top-K, the fused resolver (with
+its host-row copies) and sparse MLA for every layer of the group, then the
+one-launch page materialisation when pages complete. The default workload is a
+single request at 128K context (64 heads, 4 sparse-MLA layers sharing one
+indexer, top-K 2,048, 75 % of pages host-only, hot buffer 4,096 rows).
+
+value: query tokens/s with every step's inputs already in HBM; each step is
+timed with CUDA events and L2 is flushed (a 256 MB write) between timed steps.
+e2e: the same metric when every step copies its inputs from pinned host memory
+and its attention outputs back, inside the timed region.
+Under torchrun each rank runs its own independent request (weak scaling) and
+rank 0 reports the sum of tokens over the maximum time across ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HiSparse decode tokens/s (1 GB300) + achieved HBM/host-link GB/s vs roofline"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="ctx128k")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle's CPU sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                backend = "gloo"
+        except Exception:
+            backend = "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def workload_config(name, steps_total, rank):
+    from sparse_mla_kv_indexer_gb300 import workload as W
+    cfg = W.named_config(name)
+    return dataclasses.replace(cfg, steps=max(cfg.steps, steps_total), seed=cfg.seed + rank)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.gpu = gpu_index
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes of each hot-path call
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(cfg, plans, counters_misses_rows):
+    """Bytes each call must move at minimum, per call, averaged over the given steps.
+
+    indexer_topk: 128 B per scored key, keys read once per request (shared by its
+    query tokens); sparse_mla_decode: per query token 2,048 rows x 660 B plus
+    2,176 B of bf16 query and output per head (vLLM blog Part 2, footnote 1);
+    resolve_topk: misses x 656 B x layers over the host link; offload_pages:
+    64 x 656 B x layers per page over the host link."""
+    keys = 0
+    for p in plans:
+        per_req = {}
+        for t in p.tokens:
+            per_req[t.req] = max(per_req.get(t.req, 0), t.limit)
+        keys += sum(per_req.values())
+    keys /= len(plans)
+    n_tok = len(plans[0].tokens)
+    idx = keys * 128
+    attn = n_tok * (cfg.topk * 660 + cfg.n_heads * 2176)
+    offl = sum(len(p.offload) for p in plans) / len(plans) * 64 * 656 * cfg.n_layers
+    return {"indexer_topk": idx, "sparse_mla_decode": attn, "offload_pages": offl,
+            "resolve_topk_host_link": counters_misses_rows * 656}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_file, name):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d[name]
+        src = open(os.path.join(ROOT, "sparse_mla_kv_indexer_gb300", "csrc", kernel_file), "rb").read()
+        if ent.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return ent.get("bytes_per_launch")
+    except Exception:
+        return None
+
+
+KERNEL_FILES = {"indexer_topk": "hs_indexer.cu", "sparse_mla_decode": "hs_attention.cu",
+                "resolve_topk": "hs_resolver.cu", "offload_pages": "hs_pool.cu", "append": "hs_pool.cu"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm
+# ---------------------------------------------------------------------------
+def oracle_sample(name, seconds, rank=0):
+    """Run the CPU oracle over consecutive steps of the workload until `seconds`
+    of CPU work have been spent (at least one step). Returns (tokens/s, sample, cores)."""
+    from oracle.engine import OracleRun
+    from sparse_mla_kv_indexer_gb300 import schedule as S
+    from sparse_mla_kv_indexer_gb300 import workload as W
+    cfg = workload_config(name, 64, rank)
+    wl = W.Workload(cfg)
+    sch = S.Schedule(cfg)
+    run = OracleRun(wl, sch.setup)
+    toks = 0
+    steps = 0
+    t0 = time.perf_counter()
+    while steps < cfg.steps:
+        p = sch.plan(steps)
+        run.step(p)
+        toks += len(p.tokens)
+        steps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return toks / dt, f"{steps} consecutive decode steps of {name} ({toks} query tokens, {dt:.1f} s)", cores
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    # bounded sample per timed step: the whole run (warmup + steps) stays within minutes
+    per_step = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    values = []
+    sample = ""
+    cores = os.cpu_count() or 1
+    for i in range(args.warmup + args.steps):
+        v, sample, cores = oracle_sample(args.workload, per_step)
+        if i >= args.warmup:
+            values.append(v)
+    value = statistics.median(values) if values else 0.0
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value if value else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        rc = reference_arm(args, rank, world)
+        barrier(world)
+        return rc
+    import torch
+    from sparse_mla_kv_indexer_gb300 import build as B
+    if rank == 0 or not os.path.exists(B.LIB):
+        B.build()
+    barrier(world)
+    from sparse_mla_kv_indexer_gb300 import schedule as S
+    from sparse_mla_kv_indexer_gb300 import workload as W
+    from sparse_mla_kv_indexer_gb300.driver import BenchSession, GpuRun
+
+    torch.cuda.set_device(local)
+    K, Wm = args.steps, max(3, args.warmup)
+    total = 2 * (Wm + K)
+    cfg = workload_config(args.workload, total, rank)
+    wl = W.Workload(cfg)
+    sch = S.Schedule(cfg)
+    plans = [sch.plan(s) for s in range(total)]
+    run = GpuRun(wl, sch.setup)
+    dev_sess = BenchSession(run, plans[:Wm + K], mode="device")
+    host_sess = BenchSession(run, plans[Wm + K:], mode="host")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # ---- device-resident timing ----
+    for i in range(Wm):
+        dev_sess.tick(i)
+        dev_sess.step(i)
+    run.pool.raise_on_device_error()
+    run.pool.counters(reset=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local) if rank == 0 else None
+    step_ev = []
+    call_ev = {}
+    launches = 0
+    t_wall0 = time.perf_counter()
+    for i in range(Wm, Wm + K):
+        dev_sess.tick(i)
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dev_sess.step(i, events=call_ev)
+        b.record(stream)
+        step_ev.append((a, b))
+        launches += dev_sess.launches(i)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop() if clocks else None
+    barrier(world)
+    run.pool.raise_on_device_error()
+    counters = run.pool.counters(reset=True)
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    t_total = sum(step_ms) / 1000.0
+    t_max = max_over_ranks(t_total, world)
+    tokens = dev_sess.n_tokens * K
+    tokens_all = sum_over_ranks(tokens, world)
+    value = tokens_all / t_max
+    calls = {k: [a.elapsed_time(b) for a, b in v] for k, v in call_ev.items()}
+
+    # ---- end-to-end timing through host buffers ----
+    for i in range(Wm):
+        host_sess.tick(i)
+        host_sess.step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ev = []
+    for i in range(Wm, Wm + K):
+        host_sess.tick(i)
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        host_sess.step(i)
+        b.record(stream)
+        e2e_ev.append((a, b))
+    torch.cuda.synchronize()
+    run.pool.raise_on_device_error()
+    e2e_t = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1000.0, world)
+    e2e_value = sum_over_ranks(host_sess.n_tokens * K, world) / e2e_t
+
+    if rank != 0:
+        barrier(world)
+        return 0
+
+    # ---- roofline of the dominant call ----
+    miss_rows = counters.h2d_bytes / 656.0 / K
+    alg = algorithmic_bytes(cfg, plans[Wm:Wm + K], miss_rows)
+    share = {k: sum(v) for k, v in calls.items()}
+    dom = max(share, key=share.get)
+    avg_ms = statistics.mean(calls[dom])
+    peak, peak_kind = measured_peaks()
+    dom_bytes = alg.get(dom, 0.0)
+    achieved = dom_bytes / (avg_ms / 1000.0) / 1e9 if avg_ms > 0 else 0.0
+    step_bytes = alg["indexer_topk"] * cfg.n_groups + alg["sparse_mla_decode"] * cfg.n_layers
+    roof_step_s = step_bytes / (peak * 1e9)
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, sample, cores = oracle_sample(args.workload, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": 1000.0 * t_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8/fp8-e4m3 x fp16 tensor cores, fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "requests_per_gpu": cfg.n_requests,
+                   "context": list(cfg.ctx_len)[:4], "heads": cfg.n_heads, "topk": cfg.topk,
+                   "sparse_layers": cfg.n_layers, "indexer_layers": cfg.n_groups,
+                   "query_tokens_per_request": cfg.t_q, "l2": "flushed between timed steps (256 MB write)"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "traffic": ncu_traffic(KERNEL_FILES.get(dom, ""), dom)},
+        "step_roofline": {"algorithmic_hbm_bytes": step_bytes, "roofline_ms": roof_step_s * 1e3,
+                          "frac": roof_step_s / (t_max / K)},
+        "breakdown_ms_per_call": {k: statistics.mean(v) for k, v in calls.items()},
+        "calls_per_step": {k: len(v) / K for k, v in calls.items()},
+        "resolver": {"hits": counters.hits / K, "misses": counters.misses / K, "resident": counters.resident / K,
+                     "h2d_bytes_per_step": counters.h2d_bytes / K, "d2h_bytes_per_step": counters.d2h_bytes / K},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": statistics.mean(host_sess.h2d_bytes),
+                "d2h_bytes_per_step": host_sess.d2h_bytes},
+        "gpu_launches": launches,
+        "wall_s_timed_loop": wall,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    barrier(world)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,215 @@
+/*
+ * hisparse.h -- C ABI of the Hybrid HiSparse decode hot path on GB300 (sm_103a).
+ *
+ * One decode step of sparse-MLA attention with KV offloading, as described by
+ * "vLLM introduces Hybrid HiSparse hybrid sparse offloading for GLM 5.3"
+ * (vLLM blog Part 1; cited below as [P1]) and "Serving GLM-5.3 with PCP, DCP and
+ * Hybrid HiSparse" (vLLM blog Part 2; [P2]):
+ *
+ *   hs_append_rows        write the step's new KV rows and index keys
+ *   hs_indexer_topk       score every earlier token, keep the top K    [P2 "Why not TP or DP?"]
+ *   hs_resolve_topk       map each selected token to a KV row id       [P1 "How it works"]
+ *   hs_sparse_mla_decode  attention over only those rows               [P2 footnote 1]
+ *   hs_offload_pages      copy completed pages of all layers to host   [P1 "How it works"]
+ *
+ * Conventions
+ * - Every call returns an hs_status. No C++ exception crosses the ABI.
+ * - "d_" pointers are device memory, "h_" pointers are host memory. The big
+ *   buffers (KV pool tensors, index-key caches, pinned host pool) are owned by
+ *   the caller and must outlive the pool. The library owns only the opaque
+ *   hs_pool and its device metadata, allocated by hs_pool_init and freed by
+ *   hs_pool_destroy. No call between hs_pool_init and hs_pool_destroy
+ *   allocates device or host memory.
+ * - Hot-path calls (hs_append_rows .. hs_offload_pages) are asynchronous on the
+ *   given stream, do not synchronise with the host and read no device data on
+ *   the host, so a sequence of them can be captured in a CUDA graph. Errors the
+ *   kernels detect (bad ids, a miss with no host copy, hot-buffer overflow, a
+ *   timed-out wait) are recorded in a device status word and reported by
+ *   hs_get_error, which synchronises the stream. A call that finds a bad
+ *   argument on the host returns HS_ERR_INVALID and launches nothing.
+ * - A query-token batch is described by per-token device arrays: d_req (the
+ *   request slot of each token) and d_limit (causal limit: the token sees
+ *   positions [0, limit)). The tokens of one request are contiguous in the
+ *   batch, at most max_q_per_req of them, in ascending position.
+ * - bf16 values are passed as uint16_t bit patterns.
+ */
+#ifndef HISPARSE_H
+#define HISPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* hs_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum hs_status {
+  HS_OK = 0,
+  HS_ERR_INVALID = 1,      /* bad argument found on the host; nothing launched */
+  HS_ERR_OOM = 2,          /* hs_pool_init could not allocate its metadata */
+  HS_ERR_CAPACITY = 3,     /* device: more misses than evictable hot-buffer slots */
+  HS_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+  HS_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel gave up */
+  HS_ERR_HOST_MISSING = 6, /* device: a placeholder page without a host copy was selected */
+  HS_ERR_BAD_ID = 7,       /* device: a page, row or token id out of range */
+  HS_ERR_BAD_WEIGHT = 8    /* device: a negative index-head weight */
+} hs_status;
+
+/* Pool geometry. Sizes are fixed for the pool's lifetime. */
+typedef struct hs_pool_config {
+  int32_t page_size;          /* tokens per page; must be 64 */
+  int32_t row_bytes;          /* bytes per KV row; must be 656 ([P2] footnote 1, fp8_ds_mla) */
+  int32_t idx_dim;            /* index key dims; must be 128 */
+  int32_t n_idx_heads;        /* H_i, 1..64 */
+  int32_t n_heads;            /* attention heads H: 16, 32 or 64 */
+  int32_t topk;               /* K: multiple of 128, 128..2048 */
+  int32_t n_layers;           /* sparse-MLA layers, 1..64 */
+  int32_t layers_per_indexer; /* IndexShare group size ([P1] "Sparsity when you need it"), 1..8 */
+  int32_t num_pages;          /* pool pages in each layer's KV tensor */
+  int32_t num_idx_pages;      /* pages in each indexer layer's key cache */
+  int32_t max_requests;       /* request slots */
+  int32_t max_ctx;            /* max positions per request, multiple of 128 */
+  int32_t max_q_per_req;      /* query tokens per request per call, 1..4 */
+  int32_t hot_rows;           /* hot-buffer capacity per (request, group), multiple of 64 */
+  int32_t max_tokens;         /* query tokens per call, 1..1024 */
+  int32_t reserved;
+  int64_t host_pages;         /* pages in the pinned host pool */
+} hs_pool_config;
+
+/* One resolved selection ([P1] "How it works": resident / hot / miss). */
+typedef struct hs_plan_entry {
+  int32_t kind;    /* 0 pad (-1 in top-K), 1 resident, 2 hot-buffer hit, 3 miss */
+  int32_t slot;    /* hot-buffer slot for hit and miss, else -1 */
+  int32_t row;     /* HMA row id = pool page * 64 + offset, -1 for pad */
+  int32_t evicted; /* token whose slot a miss took over, else -1 */
+} hs_plan_entry;
+
+/* Running counters kept on the device, read by hs_get_counters. */
+typedef struct hs_counters {
+  uint64_t resident;   /* distinct selected tokens read in place */
+  uint64_t hits;       /* distinct selected tokens found in the hot buffer */
+  uint64_t misses;     /* distinct selected tokens copied from host */
+  uint64_t h2d_bytes;  /* bytes copied host -> device by misses (656 per row per layer) */
+  uint64_t d2h_bytes;  /* bytes copied device -> host by hs_offload_pages */
+  uint64_t reserved[3];
+} hs_counters;
+
+typedef struct hs_pool hs_pool;
+
+/*
+ * Create a pool over caller-owned memory.
+ *  cfg         geometry (copied).
+ *  d_kv_layers n_layers device pointers, each [num_pages, 64, 656] bytes, 16-byte aligned.
+ *              Row layout: 512 FP8 e4m3 latent, 4 fp32 scales (one per 128 latent
+ *              values), 64 bf16 rope values, little endian.
+ *  d_idx_layers ceil(n_layers / layers_per_indexer) device pointers, each
+ *              [num_idx_pages, 64, 128] int8 index keys, 16-byte aligned.
+ *  h_host_kv   pinned, mapped host memory of host_pages * n_layers * 64 * 656 bytes,
+ *              layout [host_page][layer][64][656] (cudaHostAlloc or torch pin_memory).
+ *  out         receives the pool.
+ * Allocates the per-request metadata (block tables, hot-buffer state, scratch)
+ * on the current device and initialises it: every page a placeholder, every hot
+ * buffer empty. Errors: HS_ERR_INVALID (bad geometry, null or misaligned
+ * pointer, host memory not mapped), HS_ERR_OOM, HS_ERR_CUDA.
+ */
+hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers,
+                       void* const* d_idx_layers, void* h_host_kv, hs_pool** out);
+
+/* Synchronises the device and frees everything hs_pool_init allocated. */
+hs_status hs_pool_destroy(hs_pool* pool);
+
+/* ---------------------------------------------------------------------------
+ * Host-side residency updates, issued between steps (stream-ordered copies of
+ * small host arrays; the host arrays may be reused as soon as the call returns).
+ * ------------------------------------------------------------------------- */
+
+/* Set n consecutive logical pages [first_page, first_page + n) of request req.
+ *  h_block_table  pool page or -1 (placeholder: the page lives on the host only);
+ *                 [P1] "How it works": the block table holds real blocks and
+ *                 empty placeholders.
+ *  h_idx_pages    index-key cache page of each logical page (always resident).
+ *  h_host_pages   host page holding the page's materialised copy, or -1.
+ * Any of the three may be NULL to leave that table unchanged. */
+hs_status hs_request_set_pages(hs_pool* pool, int32_t req, int32_t first_page, int32_t n,
+                               const int32_t* h_block_table, const int32_t* h_idx_pages,
+                               const int64_t* h_host_pages, hs_stream_t stream);
+
+/* Lease n more pool pages to the hot buffer of (req, group): their 64 * n slots
+ * follow the existing ones. Hot pages are ordinary pool pages from the same KV
+ * tensors ([P1] "How it works"). Total leased rows must stay <= hot_rows. */
+hs_status hs_hot_lease(hs_pool* pool, int32_t req, int32_t group, int32_t n,
+                       const int32_t* h_pool_pages, hs_stream_t stream);
+
+/* Empty every hot buffer of req (request end); the caller takes the pages back. */
+hs_status hs_hot_release(hs_pool* pool, int32_t req, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Device hot path (graph-capturable).
+ * ------------------------------------------------------------------------- */
+
+/* Write the KV row of every sparse layer and the index key of every indexer
+ * layer for n_tokens new positions.
+ *  d_req, d_pos   [n] request slot and position of each new row.
+ *  d_kv_rows      [n, n_layers, 656] bytes; d_idx_keys [n, n_idx_layers, 128] int8.
+ * The page holding each position must be resident (block table >= 0). */
+hs_status hs_append_rows(hs_pool* pool, int32_t n_tokens, const int32_t* d_req,
+                         const int32_t* d_pos, const uint8_t* d_kv_rows,
+                         const int8_t* d_idx_keys, hs_stream_t stream);
+
+/* Indexer scores and top-K for one indexer layer ([P2] "Why not TP or DP?": the
+ * indexer scores every earlier token to pick the 2,048 that sparse MLA attends to).
+ *  s[t] = sum_h w[h] * max(0, sum_d q[h][d] * key_t[d]) exact in int64, t < limit.
+ *  d_q [n, H_i, 128] int8, d_w [n, H_i] int8 (must be >= 0).
+ *  d_topk [n, K] int32 out: the K highest scores, ties to the lower token, in
+ *  ascending token order; -1 pads when limit < K.
+ *  d_scores nullable [n, max_ctx] int64 out: every score (entries >= limit undefined). */
+hs_status hs_indexer_topk(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
+                          const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
+                          const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,
+                          hs_stream_t stream);
+
+/* Fused top-K resolver for indexer group `group` at step `step` ([P1] "How it
+ * works"): for the union of the selected tokens of each request, a resident page
+ * is read in place, a hot-buffer hit refreshes its LRU stamp, and a miss takes
+ * the least recently used slot (stamp, then slot, ascending; empty slots first)
+ * and copies that token's row of every layer of the group from the pinned host
+ * pool into it. step must increase from call to call for a given (req, group).
+ *  d_topk [n, K] from hs_indexer_topk; d_row_ids [n, K] out (-1 for pads);
+ *  d_plan nullable [n, K] out. */
+hs_status hs_resolve_topk(hs_pool* pool, int32_t group, int32_t step, int32_t n_tokens,
+                          const int32_t* d_req, const int32_t* d_topk, int32_t* d_row_ids,
+                          hs_plan_entry* d_plan, hs_stream_t stream);
+
+/* Sparse MLA decode for one layer ([P2] footnote 1; MQA form: every row serves
+ * all heads). Per token and head: z_t = sm_scale * q . k_t over the 576 dims
+ * (512 dequantised latent + 64 rope) of each selected row, o = softmax(z) . v_t
+ * over the 512 latent dims, lse = log sum exp z.
+ *  d_q [n, H, 576] bf16; d_row_ids [n, K] (-1 skipped); d_out [n, H, 512] bf16;
+ *  d_lse nullable [n, H] fp32. */
+hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, int32_t n_tokens,
+                               const uint16_t* d_q, const int32_t* d_row_ids, float sm_scale,
+                               uint16_t* d_out, float* d_lse, hs_stream_t stream);
+
+/* Copy n pool pages of every sparse layer to their host pages in one launch
+ * ([P1] "How it works": all sparse-MLA layers are copied in one launch after the
+ * forward pass, ordered on the model's stream).
+ *  d_pool_pages [n] int32, d_host_pages [n] int64. */
+hs_status hs_offload_pages(hs_pool* pool, int32_t n, const int32_t* d_pool_pages,
+                           const int64_t* d_host_pages, hs_stream_t stream);
+
+/* Synchronise stream, return the first device-detected error since the last
+ * call in *device_status and clear it. */
+hs_status hs_get_error(hs_pool* pool, hs_status* device_status, hs_stream_t stream);
+
+/* Synchronise stream and read the device counters (reset = nonzero clears them). */
+hs_status hs_get_counters(hs_pool* pool, hs_counters* out, int32_t reset, hs_stream_t stream);
+
+/* Static text for a status code. */
+const char* hs_status_string(hs_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HISPARSE_H */

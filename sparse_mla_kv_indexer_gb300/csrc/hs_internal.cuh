@@ -1,0 +1,238 @@
+// Private definitions shared by the translation units of libhisparse.so:
+// pool state, geometry constants and the sm_103a PTX wrappers (mbarrier,
+// bulk copies, tcgen05 tensor-core and tensor-memory instructions).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "hisparse.h"
+
+namespace hs {
+
+constexpr int PAGE = 64;           // tokens per page
+constexpr int ROW = 656;           // bytes per KV row
+constexpr int ROW_CHUNKS = 41;     // 16-byte chunks per row
+constexpr int LATENT = 512;        // FP8 latent dims
+constexpr int ROPE = 64;           // bf16 rope dims
+constexpr int QK = 576;            // QK dims
+constexpr int IDX_DIM = 128;       // index key dims
+constexpr int IDX_PAGE_BYTES = PAGE * IDX_DIM;
+constexpr int ATTN_ROWS = 128;     // selected rows per attention CTA (MMA M)
+constexpr int MAX_SPLITS = 16;     // 2048 / 128
+constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded device waits: 1 s
+
+// Device-side view of a pool (passed by value to kernels).
+struct Dev {
+  // geometry
+  int32_t n_idx_heads, n_heads, topk, n_layers, lpi, n_groups;
+  int32_t num_pages, num_idx_pages, max_requests, max_ctx, max_pages;
+  int32_t max_q, hot_rows, hot_pages_max, max_tokens;
+  int64_t host_pages;
+  // residency metadata
+  int32_t* bt;          // [max_requests, max_pages] pool page or -1
+  int32_t* idx_bt;      // [max_requests, max_pages] index-cache page
+  int64_t* host_pg;     // [max_requests, max_pages] host page or -1
+  int32_t* hot_pages;   // [max_requests, n_groups, hot_pages_max]
+  int32_t* n_hot;       // [max_requests, n_groups] leased pages
+  int32_t* slot_token;  // [max_requests, n_groups, hot_rows]
+  int32_t* slot_stamp;  // [max_requests, n_groups, hot_rows]
+  int32_t* tok2slot;    // [max_requests, n_groups, max_ctx]
+  // caller-owned data
+  uint8_t** kv;         // [n_layers] device pointers
+  int8_t** idx;         // [n_groups] device pointers
+  uint8_t* host;        // device alias of the pinned host pool
+  // status and counters
+  int32_t* status;
+  unsigned long long* counters;   // resident, hits, misses, h2d, d2h
+  // scratch
+  int64_t* scores;      // [max_tokens, max_ctx]
+  int4* miss_list;      // [max_tokens * topk] (layer-group row copies): {req, token, dst_row, 0}
+  int32_t* miss_count;  // [max_tokens] misses recorded by the segment starting at each token
+  float* o_part;        // [max_tokens, MAX_SPLITS, n_heads, 512]
+  float2* ml_part;      // [max_tokens, MAX_SPLITS, n_heads] (max, sum) in log2 units
+};
+
+enum Counter { C_RESIDENT = 0, C_HITS = 1, C_MISSES = 2, C_H2D = 3, C_D2H = 4, C_N = 8 };
+
+}  // namespace hs
+
+struct hs_pool {
+  hs_pool_config cfg;
+  hs::Dev d;
+  int device;
+  std::vector<int32_t> n_hot_host;   // leased pages per (req, group), mirrored on the host
+  std::vector<void*> allocations;
+};
+
+namespace hs {
+
+// ---- error helpers ---------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t* st, int code) {
+  atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier ----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of a barrier, giving up after WAIT_NS and recording
+// HS_ERR_TIMEOUT. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > WAIT_NS) {
+        set_status(status, HS_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ---- bulk copies (TMA unit, untiled) ------------------------------------------
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- tcgen05 ---------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] x B[smem desc], kind::f16, issued by one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on an mbarrier once every tcgen05.mma issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Each thread of the warp reads 32 consecutive fp32 columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
+//  K-major operand: rows of 128 B (64 16-bit elements), 8-row groups `sbo` apart.
+//  MN-major operand: 128-B lines of 64 MN elements, 8 K-lines per group `sbo`
+//  apart, 64-element MN blocks `lbo` apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;          // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;          // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16 with fp16 A and B and fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)                                   // D = f32
+         | (0u << 7) | (0u << 10)                    // A, B = f16
+         | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16)
+         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Byte offset of 16-bit element (row, col) inside a [rows x 64] SW128 block
+// (row-major 128-B lines, 16-B chunks XOR-swizzled by row % 8).
+__host__ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+  return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7)) & 7) << 4) + ((col & 7) << 1));
+}
+// Byte offset of the 16-B chunk `chunk` (0..7) of line `row`.
+__host__ __device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
+  return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
+}
+
+// ---- host-side launch helpers (defined in hs_pool.cu) ----------------------------
+hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
+                         const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, cudaStream_t st);
+hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                        int32_t* d_topk, cudaStream_t st);
+hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* d_req,
+                         const int32_t* d_topk, int32_t* d_row_ids, hs_plan_entry* d_plan,
+                         cudaStream_t st);
+hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows,
+                           float sm_scale, uint16_t* d_out, float* d_lse, cudaStream_t st);
+int num_sms();
+
+}  // namespace hs

@@ -1,0 +1,254 @@
+"""Synthetic decode-step driver over the C ABI.
+
+Stands in for the serving engine around the hot path: it owns the caller-side
+buffers (KV pool tensors, index caches, pinned host pool), fills them from a
+seeded workload, applies the host residency schedule between steps and issues
+the hot-path calls of each step:
+
+    append -> per indexer group: indexer_topk -> resolve_topk -> sparse_mla_decode per layer
+           -> offload_pages (all layers, one launch)
+
+Every computation runs in libhisparse.so; this module only moves inputs to the
+device and results back.
+"""
+from __future__ import annotations
+
+from typing import Dict, List
+
+import numpy as np
+
+from . import hisparse as H
+from .schedule import Setup, StepPlan
+from .workload import IDX_DIM, PAGE, ROW_BYTES, Workload
+
+PLAN_FIELDS = 4
+
+
+def pool_config(wl: Workload, setup: Setup) -> H.PoolConfig:
+    cfg = wl.cfg
+    max_ctx = -(-setup.n_pages_max * PAGE // 128) * 128
+    return H.PoolConfig(
+        page_size=PAGE, row_bytes=ROW_BYTES, idx_dim=IDX_DIM, n_idx_heads=cfg.n_idx_heads,
+        n_heads=cfg.n_heads, topk=cfg.topk, n_layers=cfg.n_layers,
+        layers_per_indexer=cfg.layers_per_indexer, num_pages=setup.num_pages,
+        num_idx_pages=setup.num_idx_pages, max_requests=cfg.n_requests, max_ctx=max_ctx,
+        max_q_per_req=cfg.t_q, hot_rows=cfg.hot_rows, max_tokens=cfg.n_requests * cfg.t_q,
+        reserved=0, host_pages=setup.host_pages)
+
+
+class GpuRun:
+    def __init__(self, wl: Workload, setup: Setup, keep_scores: bool = False, device: str = "cuda"):
+        import torch
+        self.torch = torch
+        self.wl = wl
+        self.cfg = cfg = wl.cfg
+        self.setup = setup
+        self.keep_scores = keep_scores
+        self.dev = torch.device(device)
+        self.pc = pool_config(wl, setup)
+        self.max_ctx = self.pc.max_ctx
+        R, L, G = cfg.n_requests, cfg.n_layers, cfg.n_groups
+        npg, nip = setup.num_pages, setup.num_idx_pages
+        # host-side staging of the initial contents
+        pool_np = [np.zeros((npg * PAGE, ROW_BYTES), np.uint8) for _ in range(L)]
+        idx_np = [np.zeros((nip * PAGE, IDX_DIM), np.int8) for _ in range(G)]
+        self.host = torch.zeros(setup.host_pages * L * PAGE * ROW_BYTES, dtype=torch.uint8, pin_memory=True)
+        host_np = self.host.numpy().reshape(setup.host_pages, L, PAGE, ROW_BYTES)
+        for r in range(R):
+            P = setup.prefix_len[r]
+            for l in range(L):
+                rows = wl.kv_rows(r, l)
+                for p in range(-(-P // PAGE)):
+                    lo, hi = p * PAGE, min(P, (p + 1) * PAGE)
+                    if setup.block_table[r, p] >= 0:
+                        b = int(setup.block_table[r, p]) * PAGE
+                        pool_np[l][b:b + hi - lo] = rows[lo:hi]
+                    if setup.materialised[r, p]:
+                        host_np[setup.host_page[r, p], l, :hi - lo] = rows[lo:hi]
+            for g in range(G):
+                keys = wl.idx_keys(r, g)
+                for p in range(-(-P // PAGE)):
+                    lo, hi = p * PAGE, min(P, (p + 1) * PAGE)
+                    b = int(setup.idx_page[r, p]) * PAGE
+                    idx_np[g][b:b + hi - lo] = keys[lo:hi]
+        self.kv = [torch.from_numpy(a.reshape(-1)).to(self.dev) for a in pool_np]
+        self.idx = [torch.from_numpy(a.reshape(-1)).to(self.dev) for a in idx_np]
+        del pool_np, idx_np
+        self.pool = H.Pool(self.pc, self.kv, self.idx, self.host)
+        for r in range(R):
+            self.pool.set_pages(r, 0, block_table=setup.block_table[r].tolist(),
+                                idx_pages=setup.idx_page[r].tolist(), host_pages=setup.host_page[r].tolist())
+        for (r, g, pages) in setup.leases:
+            self.pool.hot_lease(r, g, pages)
+        torch.cuda.synchronize()
+
+    # ------------------------------------------------------------------
+    def apply_tick(self, tick) -> None:
+        for (r, p, pg) in tick.bt_set:
+            self.pool.set_pages(r, p, block_table=[pg])
+        for r in tick.releases:
+            self.pool.hot_release(r)
+        for (r, g, pages) in tick.leases:
+            self.pool.hot_lease(r, g, pages)
+
+    def step_inputs(self, plan: StepPlan) -> Dict[str, np.ndarray]:
+        """Host arrays of one step, in batch order (tokens grouped by request)."""
+        cfg, wl, s = self.cfg, self.wl, plan.step
+        toks = plan.tokens
+        t_q = cfg.t_q
+        out = {
+            "req": np.array([t.req for t in toks], np.int32),
+            "pos": np.array([t.pos for t in toks], np.int32),
+            "limit": np.array([t.limit for t in toks], np.int32),
+            "kv_rows": np.stack([np.stack([wl.kv_rows(t.req, l)[t.pos] for l in range(cfg.n_layers)]) for t in toks]),
+            "idx_keys": np.stack([np.stack([wl.idx_keys(t.req, g)[t.pos] for g in range(cfg.n_groups)])
+                                  for t in toks]),
+            "q_idx": np.stack([np.stack([wl.idx_queries(t.req, g, s)[i % t_q] for i, t in enumerate(toks)])
+                               for g in range(cfg.n_groups)]),
+            "w_idx": np.stack([np.stack([wl.idx_weights(t.req, g) for t in toks]) for g in range(cfg.n_groups)]),
+            "q_attn": np.stack([np.stack([wl.attn_queries(t.req, l, s)[i % t_q] for i, t in enumerate(toks)])
+                                for l in range(cfg.n_layers)]),
+            "off_pool": np.array([o[2] for o in plan.offload], np.int32),
+            "off_host": np.array([o[3] for o in plan.offload], np.int64),
+        }
+        return out
+
+    def step(self, plan: StepPlan, collect: bool = True) -> Dict[str, object]:
+        torch = self.torch
+        cfg, dev = self.cfg, self.dev
+        self.apply_tick(plan.tick)
+        x = self.step_inputs(plan)
+        n = len(plan.tokens)
+        K = cfg.topk
+        req = torch.from_numpy(x["req"]).to(dev)
+        pos = torch.from_numpy(x["pos"]).to(dev)
+        limit = torch.from_numpy(x["limit"]).to(dev)
+        self.pool.append_rows(req, pos, torch.from_numpy(x["kv_rows"]).to(dev),
+                              torch.from_numpy(x["idx_keys"]).to(dev))
+        res = {"topk": [], "row_ids": [], "plan": [], "scores": [], "o": [None] * cfg.n_layers,
+               "lse": [None] * cfg.n_layers}
+        for g in range(cfg.n_groups):
+            q = torch.from_numpy(np.ascontiguousarray(x["q_idx"][g])).to(dev)
+            w = torch.from_numpy(np.ascontiguousarray(x["w_idx"][g])).to(dev)
+            topk = torch.empty((n, K), dtype=torch.int32, device=dev)
+            scores = torch.empty((n, self.max_ctx), dtype=torch.int64, device=dev) if self.keep_scores else None
+            self.pool.indexer_topk(g, req, limit, q, w, topk, scores)
+            row_ids = torch.empty((n, K), dtype=torch.int32, device=dev)
+            plan_t = torch.empty((n, K, PLAN_FIELDS), dtype=torch.int32, device=dev)
+            self.pool.resolve_topk(g, plan.step, req, topk, row_ids, plan_t)
+            for l in cfg.group_layers(g):
+                qa = torch.from_numpy(np.ascontiguousarray(x["q_attn"][l]).view(np.int16)).to(dev)
+                o = torch.empty((n, cfg.n_heads, 512), dtype=torch.int16, device=dev)
+                lse = torch.empty((n, cfg.n_heads), dtype=torch.float32, device=dev)
+                self.pool.sparse_mla_decode(l, qa, row_ids, self.wl.sm_scale(), o, lse)
+                if collect:
+                    res["o"][l] = o.view(torch.bfloat16).float().cpu().numpy()
+                    res["lse"][l] = lse.cpu().numpy()
+            if collect:
+                res["topk"].append(topk.cpu().numpy())
+                res["row_ids"].append(row_ids.cpu().numpy())
+                res["plan"].append(plan_t.cpu().numpy())
+                res["scores"].append(scores.cpu().numpy() if scores is not None else None)
+        if len(plan.offload):
+            self.pool.offload_pages(torch.from_numpy(x["off_pool"]).to(dev), torch.from_numpy(x["off_host"]).to(dev))
+        res["status"] = self.pool.get_error()
+        return res
+
+    def host_pages_view(self) -> np.ndarray:
+        L = self.cfg.n_layers
+        return self.host.numpy().reshape(self.setup.host_pages, L, PAGE, ROW_BYTES)
+
+    def pool_rows(self, layer: int) -> np.ndarray:
+        return self.kv[layer].cpu().numpy().reshape(-1, ROW_BYTES)
+
+    def close(self) -> None:
+        self.pool.close()
+
+
+class BenchSession:
+    """Runs decode steps with every step's inputs staged ahead of time.
+
+    device mode: inputs of all steps sit in HBM before timing starts; a step is
+    only the hot-path calls.  host mode: inputs sit in pinned host buffers and
+    each step copies its inputs host -> device and its attention outputs
+    device -> host on the same stream, inside the timed region.
+    """
+
+    def __init__(self, run: GpuRun, plans, mode: str = "device"):
+        import torch
+        self.torch = torch
+        self.run = run
+        self.plans = plans
+        self.mode = mode
+        cfg = run.cfg
+        dev = run.dev
+        self.steps = []
+        for plan in plans:
+            x = run.step_inputs(plan)
+            arrays = {
+                "req": x["req"], "pos": x["pos"], "limit": x["limit"],
+                "kv_rows": x["kv_rows"], "idx_keys": x["idx_keys"],
+                "q_idx": x["q_idx"], "w_idx": x["w_idx"],
+                "q_attn": x["q_attn"].view(np.int16),
+                "off_pool": x["off_pool"], "off_host": x["off_host"],
+            }
+            host = {k: torch.from_numpy(np.ascontiguousarray(v)) for k, v in arrays.items()}
+            if mode == "host":
+                host = {k: v.pin_memory() for k, v in host.items()}
+                devt = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+            else:
+                devt = {k: v.to(dev) for k, v in host.items()}
+            self.steps.append((plan, host, devt))
+        n = cfg.n_requests * cfg.t_q
+        self.n_tokens = n
+        K = cfg.topk
+        self.topk = [torch.empty((n, K), dtype=torch.int32, device=dev) for _ in range(cfg.n_groups)]
+        self.row_ids = [torch.empty((n, K), dtype=torch.int32, device=dev) for _ in range(cfg.n_groups)]
+        self.out = torch.empty((cfg.n_layers, n, cfg.n_heads, 512), dtype=torch.int16, device=dev)
+        self.out_host = torch.empty_like(self.out, device="cpu").pin_memory() if mode == "host" else None
+        self.h2d_bytes = [sum(v.numel() * v.element_size() for v in h.values()) for _, h, _ in self.steps]
+        self.d2h_bytes = self.out.numel() * self.out.element_size() if mode == "host" else 0
+
+    def launches(self, i: int) -> int:
+        """Kernels one step launches (append, indexer + select, resolve + copy,
+        attention + merge per layer, offload when pages complete)."""
+        cfg = self.run.cfg
+        plan = self.steps[i][0]
+        return 1 + cfg.n_groups * 4 + cfg.n_layers * 2 + (1 if len(plan.offload) else 0)
+
+    def tick(self, i: int) -> None:
+        self.run.apply_tick(self.steps[i][0].tick)
+
+    def step(self, i: int, events=None) -> None:
+        """Issue step i on the current stream. events: optional dict name -> list of
+        (start, end) CUDA event pairs to time each hot-path call."""
+        torch = self.torch
+        run, cfg = self.run, self.run.cfg
+        plan, host, d = self.steps[i]
+        pool = run.pool
+
+        def timed(name, fn):
+            if events is None:
+                fn()
+                return
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            events.setdefault(name, []).append((a, b))
+
+        if self.mode == "host":
+            for k in d:
+                d[k].copy_(host[k], non_blocking=True)
+        timed("append", lambda: pool.append_rows(d["req"], d["pos"], d["kv_rows"], d["idx_keys"]))
+        for g in range(cfg.n_groups):
+            timed("indexer_topk", lambda: pool.indexer_topk(g, d["req"], d["limit"], d["q_idx"][g], d["w_idx"][g],
+                                                            self.topk[g]))
+            timed("resolve_topk", lambda: pool.resolve_topk(g, plan.step, d["req"], self.topk[g], self.row_ids[g]))
+            for l in cfg.group_layers(g):
+                timed("sparse_mla_decode", lambda: pool.sparse_mla_decode(l, d["q_attn"][l], self.row_ids[g],
+                                                                          run.wl.sm_scale(), self.out[l]))
+        if len(plan.offload):
+            timed("offload_pages", lambda: pool.offload_pages(d["off_pool"], d["off_host"]))
+        if self.mode == "host":
+            self.out_host.copy_(self.out, non_blocking=True)

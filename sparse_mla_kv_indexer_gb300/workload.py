@@ -31,6 +31,8 @@ step to step. Query drift: q_t = clamp(q_{t-1} + round(N(0, 4^2))).
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 from typing import Dict, List, Tuple
 
@@ -45,6 +47,7 @@ IDX_DIM = 128
 GROUP = 128
 SCALE_OFF = LATENT
 ROPE_OFF = LATENT + 16
+KV_CHUNK = 1 << 15
 
 
 # --------------------------------------------------------------------------
@@ -165,9 +168,9 @@ CONFIG_NAMES = ("tiny", "ctx128k", "batch32", "ctx1m", "multiturn")
 # Element encodings used to synthesise inputs
 # --------------------------------------------------------------------------
 def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    """float32 -> bf16 bit patterns (uint16), round to nearest even (finite inputs)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    b = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return b.astype(np.uint16)
 
 
@@ -181,22 +184,19 @@ def encode_e4m3(v: np.ndarray) -> np.ndarray:
 
     e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
     subnormal (m * 2^-9); the all-ones code 0x7F / 0xFF is NaN, so the largest
-    finite magnitude is 1.75 * 2^8 = 448.
+    finite magnitude is 1.75 * 2^8 = 448. Normal values are rounded on the
+    binary32 bit pattern (keep 3 of 23 mantissa bits, ties to even, rebias the
+    exponent from 127 to 7); magnitudes below 2^-6 are multiples of 2^-9.
     """
-    v = np.asarray(v, dtype=np.float32)
-    sign = (np.signbit(v)).astype(np.uint8) << 7
-    a = np.minimum(np.abs(v).astype(np.float64), 448.0)
-    mant, ex = np.frexp(a)                # a = mant * 2^ex, mant in [0.5, 1)
-    e = ex.astype(np.int64) - 1           # a = (2 mant) * 2^e
-    normal = (e >= -6) & (a > 0)
-    frac = np.where(normal, (2.0 * mant - 1.0) * 8.0, 0.0)
-    m = np.rint(frac).astype(np.int64)
-    carry = m == 8
-    e = np.where(carry, e + 1, e)
-    m = np.where(carry, 0, m)
-    code_n = ((e + 7) << 3) | m
-    code_s = np.rint(a * 512.0).astype(np.int64)   # subnormal: multiples of 2^-9 (8 -> 0x08)
-    code = np.where(normal, code_n, code_s).astype(np.uint8)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    b = v.view(np.uint32)
+    sign = ((b >> np.uint32(31)).astype(np.uint8)) << np.uint8(7)
+    a = b & np.uint32(0x7FFFFFFF)
+    r = (a + np.uint32(0x7FFFF) + ((a >> np.uint32(20)) & np.uint32(1))) >> np.uint32(20)
+    code_n = np.minimum(r.astype(np.int64) - (120 << 3), 0x7E)
+    sub = a < np.uint32(0x3C800000)                     # |v| < 2^-6
+    code_s = np.rint(np.abs(v).astype(np.float64) * 512.0).astype(np.int64)
+    code = np.where(sub, code_s, code_n).astype(np.uint8)
     return code | sign
 
 
@@ -259,18 +259,32 @@ class Workload:
 
     # -- KV rows --------------------------------------------------------------
     def kv_rows(self, r: int, layer: int) -> np.ndarray:
-        """[final_len, 656] uint8: the KV row of every position of request r, layer."""
+        """[final_len, 656] uint8: the KV row of every position of request r, layer.
+
+        Rows are drawn in chunks of 32,768 positions, each chunk from its own
+        seed, so chunks are generated in parallel and are independent of how
+        long the run is."""
         key = (r, layer)
         if key not in self._kv:
             n = self.cfg.final_len(r)
-            rng = _rng(self.cfg.request_seed(r), 2, layer)
             out = np.empty((n, ROW_BYTES), dtype=np.uint8)
-            chunk = 1 << 15
-            for lo in range(0, n, chunk):
-                hi = min(n, lo + chunk)
-                x = rng.standard_normal((hi - lo, QK_DIM), dtype=np.float32)
+            seed = self.cfg.request_seed(r)
+
+            def fill(ci: int) -> None:
+                lo = ci * KV_CHUNK
+                hi = min(n, lo + KV_CHUNK)
+                rng = _rng(seed, 2, layer, ci)
+                x = rng.standard_normal((KV_CHUNK, QK_DIM), dtype=np.float32)[:hi - lo]
                 x = bf16_bits_to_f32(round_to_bf16_bits(x))
                 out[lo:hi] = quantise_rows(x)
+
+            chunks = range(-(-n // KV_CHUNK))
+            if len(chunks) > 1:
+                with ThreadPoolExecutor(max_workers=min(len(chunks), os.cpu_count() or 1)) as ex:
+                    list(ex.map(fill, chunks))
+            else:
+                for ci in chunks:
+                    fill(ci)
             self._kv[key] = out
         return self._kv[key]
 

@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports every symbol include/hisparse.h
+declares; host-side argument checks answer HS_ERR_INVALID without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hisparse.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_mla_kv_indexer_gb300 import build
+    path = build.LIB
+    if not os.path.exists(path):
+        build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hs_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for want in ["hs_pool_init", "hs_pool_destroy", "hs_indexer_topk", "hs_resolve_topk",
+                 "hs_sparse_mla_decode", "hs_offload_pages", "hs_get_error", "hs_append_rows",
+                 "hs_request_set_pages", "hs_hot_lease", "hs_hot_release", "hs_get_counters",
+                 "hs_status_string"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_status_strings(lib):
+    lib.hs_status_string.restype = ctypes.c_char_p
+    assert lib.hs_status_string(0) == b"ok"
+    assert lib.hs_status_string(3) == b"hot buffer capacity exceeded"
+    assert lib.hs_status_string(99) == b"unknown status"
+
+
+def test_null_pool_is_invalid(lib):
+    P = ctypes.c_void_p
+    assert lib.hs_pool_destroy(None) == 1
+    assert lib.hs_hot_release(None, 0, None) == 1
+    assert lib.hs_indexer_topk(None, 0, 1, P(1), P(1), P(1), P(1), P(1), None, None) == 1
+    assert lib.hs_resolve_topk(None, 0, 0, 1, P(1), P(1), P(1), None, None) == 1
+    assert lib.hs_sparse_mla_decode(None, 0, 1, P(16), P(16), ctypes.c_float(1.0), P(16), None, None) == 1
+    assert lib.hs_offload_pages(None, 1, P(1), P(1), None) == 1
+    st = ctypes.c_int(0)
+    assert lib.hs_get_error(None, ctypes.byref(st), None) == 1
+
+
+def test_bad_geometry_is_invalid(lib):
+    from sparse_mla_kv_indexer_gb300.hisparse import PoolConfig
+    good = dict(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=64, n_heads=64, topk=2048,
+                n_layers=4, layers_per_indexer=4, num_pages=100, num_idx_pages=100, max_requests=1,
+                max_ctx=4096, max_q_per_req=1, hot_rows=4096, max_tokens=1, reserved=0, host_pages=10)
+    ptrs = (ctypes.c_void_p * 8)(*([16] * 8))
+    out = ctypes.c_void_p()
+    for key, bad in [("page_size", 32), ("row_bytes", 640), ("idx_dim", 64), ("n_heads", 48),
+                     ("topk", 100), ("topk", 4096), ("max_ctx", 1000), ("hot_rows", 100),
+                     ("max_q_per_req", 5), ("max_tokens", 0), ("n_idx_heads", 8)]:
+        cfg = PoolConfig(**{**good, key: bad})
+        assert lib.hs_pool_init(ctypes.byref(cfg), ptrs, ptrs, ctypes.c_void_p(16), ctypes.byref(out)) == 1, key
+    cfg = PoolConfig(**good)
+    misaligned = (ctypes.c_void_p * 8)(*([24] * 8))
+    assert lib.hs_pool_init(ctypes.byref(cfg), misaligned, ptrs, ctypes.c_void_p(16), ctypes.byref(out)) == 1
