@@ -169,8 +169,9 @@ def algorithmic_bytes(cfg, plans, counters_misses_rows):
     idx = keys * 128
     attn = n_tok * (cfg.topk * 660 + cfg.n_heads * 2176)
     offl = sum(len(p.offload) for p in plans) / len(plans) * 64 * 656 * cfg.n_layers
-    return {"indexer_topk": idx, "sparse_mla_decode": attn, "offload_pages": offl,
-            "resolve_topk_host_link": counters_misses_rows * 656}
+    append = n_tok * (cfg.n_layers * 656 + cfg.n_groups * 128) * 2
+    return {"indexer_topk": idx, "sparse_mla_decode": attn, "offload_pages": offl, "append": append,
+            "resolve_topk": counters_misses_rows * 656 + n_tok * cfg.topk * 8}
 
 
 def measured_peaks():
@@ -205,50 +206,61 @@ KERNEL_FILES = {"indexer_topk": "hs_indexer.cu", "sparse_mla_decode": "hs_attent
 # ---------------------------------------------------------------------------
 # CPU oracle arm
 # ---------------------------------------------------------------------------
+class OracleArm:
+    """The CPU oracle run over consecutive decode steps of a workload (set up once)."""
+
+    def __init__(self, name, steps, rank=0):
+        from oracle.engine import OracleRun
+        from sparse_mla_kv_indexer_gb300 import schedule as S
+        from sparse_mla_kv_indexer_gb300 import workload as W
+        self.cfg = workload_config(name, steps, rank)
+        self.sch = S.Schedule(self.cfg)
+        self.run = OracleRun(W.Workload(self.cfg), self.sch.setup)
+        self.next = 0
+        self.cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+    def step(self):
+        """One decode step; returns (query tokens, seconds)."""
+        p = self.sch.plan(self.next)
+        self.next += 1
+        t0 = time.perf_counter()
+        self.run.step(p)
+        return len(p.tokens), time.perf_counter() - t0
+
+
 def oracle_sample(name, seconds, rank=0):
-    """Run the CPU oracle over consecutive steps of the workload until `seconds`
-    of CPU work have been spent (at least one step). Returns (tokens/s, sample, cores)."""
-    from oracle.engine import OracleRun
-    from sparse_mla_kv_indexer_gb300 import schedule as S
-    from sparse_mla_kv_indexer_gb300 import workload as W
-    cfg = workload_config(name, 64, rank)
-    wl = W.Workload(cfg)
-    sch = S.Schedule(cfg)
-    run = OracleRun(wl, sch.setup)
+    """The oracle over consecutive steps until `seconds` of CPU work (at least one
+    step). Returns (tokens/s, sample description, cores)."""
+    arm = OracleArm(name, 64, rank)
     toks = 0
-    steps = 0
-    t0 = time.perf_counter()
-    while steps < cfg.steps:
-        p = sch.plan(steps)
-        run.step(p)
-        toks += len(p.tokens)
-        steps += 1
-        if time.perf_counter() - t0 >= seconds:
+    dt = 0.0
+    while arm.next < arm.cfg.steps:
+        n, t = arm.step()
+        toks += n
+        dt += t
+        if dt >= seconds:
             break
-    dt = time.perf_counter() - t0
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return toks / dt, f"{steps} consecutive decode steps of {name} ({toks} query tokens, {dt:.1f} s)", cores
+    return toks / dt, f"{arm.next} consecutive decode steps of {name} ({toks} query tokens, {dt:.1f} s)", arm.cores
 
 
 def reference_arm(args, rank, world):
     if rank != 0:
         return 0
-    # bounded sample per timed step: the whole run (warmup + steps) stays within minutes
-    per_step = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
-    values = []
-    sample = ""
-    cores = os.cpu_count() or 1
+    arm = OracleArm(args.workload, args.warmup + args.steps, rank)
+    times, toks = [], 0
     for i in range(args.warmup + args.steps):
-        v, sample, cores = oracle_sample(args.workload, per_step)
+        n, t = arm.step()
         if i >= args.warmup:
-            values.append(v)
-    value = statistics.median(values) if values else 0.0
+            times.append(t)
+            toks += n
+    value = toks / sum(times) if times else 0.0
+    sample = f"each step is one full decode step of {args.workload} ({toks // max(1, len(times))} query tokens)"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value if value else None,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * sum(times) / max(1, len(times)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": arm.cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
