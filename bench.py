@@ -47,6 +47,7 @@ def parse_args():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle's CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-call-timing", action="store_true", help="skip the single-call graph timings")
     return ap.parse_args()
 
 
@@ -204,6 +205,58 @@ KERNEL_FILES = {"indexer_topk": "hs_indexer.cu", "sparse_mla_decode": "hs_attent
 
 
 # ---------------------------------------------------------------------------
+# CUDA graphs
+# ---------------------------------------------------------------------------
+def capture(torch, fn):
+    """Capture the hot-path calls issued by fn into a CUDA graph (nothing executes)."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
+def time_calls(torch, sess, i, flush, stream, reps=20):
+    """Average device time of each hot-path call of step i, each captured alone in a
+    graph and replayed `reps` times after an L2 flush. Replaying a call whose inputs
+    are unchanged recomputes the same result (the resolver then finds every
+    selected token resident or hot)."""
+    cfg = sess.run.cfg
+    plan, host, d = sess.steps[i]
+    pool = sess.run.pool
+    g0, l0 = 0, cfg.group_layers(0)[0]
+    fns = {
+        "append": lambda: pool.append_rows(d["req"], d["pos"], d["kv_rows"], d["idx_keys"]),
+        "indexer_topk": lambda: pool.indexer_topk(g0, d["req"], d["limit"], d["q_idx"][g0], d["w_idx"][g0],
+                                                  sess.topk[g0]),
+        "resolve_topk": lambda: pool.resolve_topk(g0, plan.step, d["req"], sess.topk[g0], sess.row_ids[g0]),
+        "sparse_mla_decode": lambda: pool.sparse_mla_decode(l0, d["q_attn"][l0], sess.row_ids[g0],
+                                                            sess.run.wl.sm_scale(), sess.out[l0]),
+    }
+    if len(plan.offload):
+        fns["offload_pages"] = lambda: pool.offload_pages(d["off_pool"], d["off_host"])
+    per_step = {"append": 1, "indexer_topk": cfg.n_groups, "resolve_topk": cfg.n_groups,
+                "sparse_mla_decode": cfg.n_layers, "offload_pages": 1}
+    out = {}
+    for name, fn in fns.items():
+        g = capture(torch, fn)
+        ev = []
+        for r in range(reps):
+            flush.fill_(r & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        out[name] = {"ms": statistics.mean(a.elapsed_time(b) for a, b in ev), "per_step": per_step[name]}
+        del g
+    return out
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle arm
 # ---------------------------------------------------------------------------
 class OracleArm:
@@ -297,17 +350,18 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    # ---- device-resident timing ----
+    # ---- device-resident timing: one captured CUDA graph per step ----
     for i in range(Wm):
         dev_sess.tick(i)
         dev_sess.step(i)
     run.pool.raise_on_device_error()
+    torch.cuda.synchronize()
+    graphs = {i: capture(torch, lambda i=i: dev_sess.step(i)) for i in range(Wm, Wm + K)}
     run.pool.counters(reset=True)
     torch.cuda.synchronize()
     barrier(world)
     clocks = ClockSampler(local) if rank == 0 else None
     step_ev = []
-    call_ev = {}
     launches = 0
     t_wall0 = time.perf_counter()
     for i in range(Wm, Wm + K):
@@ -315,7 +369,7 @@ def main():
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        dev_sess.step(i, events=call_ev)
+        graphs[i].replay()
         b.record(stream)
         step_ev.append((a, b))
         launches += dev_sess.launches(i)
@@ -325,19 +379,23 @@ def main():
     barrier(world)
     run.pool.raise_on_device_error()
     counters = run.pool.counters(reset=True)
+    del graphs
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     t_total = sum(step_ms) / 1000.0
     t_max = max_over_ranks(t_total, world)
     tokens = dev_sess.n_tokens * K
     tokens_all = sum_over_ranks(tokens, world)
     value = tokens_all / t_max
-    calls = {k: [a.elapsed_time(b) for a, b in v] for k, v in call_ev.items()}
 
-    # ---- end-to-end timing through host buffers ----
+    # ---- each hot-path call alone, replayed from a single-call graph (L2 flushed) ----
+    calls = {} if args.no_call_timing else time_calls(torch, dev_sess, Wm + K - 1, flush, stream, reps=20)
+
+    # ---- end-to-end through host buffers: copies in, step, copy out, one graph per step ----
     for i in range(Wm):
         host_sess.tick(i)
         host_sess.step(i)
     torch.cuda.synchronize()
+    hgraphs = {i: capture(torch, lambda i=i: host_sess.step(i)) for i in range(Wm, Wm + K)}
     barrier(world)
     e2e_ev = []
     for i in range(Wm, Wm + K):
@@ -345,11 +403,12 @@ def main():
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        host_sess.step(i)
+        hgraphs[i].replay()
         b.record(stream)
         e2e_ev.append((a, b))
     torch.cuda.synchronize()
     run.pool.raise_on_device_error()
+    del hgraphs
     e2e_t = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1000.0, world)
     e2e_value = sum_over_ranks(host_sess.n_tokens * K, world) / e2e_t
 
@@ -360,9 +419,9 @@ def main():
     # ---- roofline of the dominant call ----
     miss_rows = counters.h2d_bytes / 656.0 / K
     alg = algorithmic_bytes(cfg, plans[Wm:Wm + K], miss_rows)
-    share = {k: sum(v) for k, v in calls.items()}
+    share = {k: v["ms"] * v["per_step"] for k, v in calls.items()} or {"sparse_mla_decode": 0.0}
     dom = max(share, key=share.get)
-    avg_ms = statistics.mean(calls[dom])
+    avg_ms = calls[dom]["ms"] if calls else 0.0
     peak, peak_kind = measured_peaks()
     dom_bytes = alg.get(dom, 0.0)
     achieved = dom_bytes / (avg_ms / 1000.0) / 1e9 if avg_ms > 0 else 0.0
@@ -389,8 +448,9 @@ def main():
                      "traffic": ncu_traffic(KERNEL_FILES.get(dom, ""), dom)},
         "step_roofline": {"algorithmic_hbm_bytes": step_bytes, "roofline_ms": roof_step_s * 1e3,
                           "frac": roof_step_s / (t_max / K)},
-        "breakdown_ms_per_call": {k: statistics.mean(v) for k, v in calls.items()},
-        "calls_per_step": {k: len(v) / K for k, v in calls.items()},
+        "breakdown_ms_per_call": {k: v["ms"] for k, v in calls.items()},
+        "calls_per_step": {k: v["per_step"] for k, v in calls.items()},
+        "timing": "each timed step is one CUDA graph replay; per-call times from single-call graphs",
         "resolver": {"hits": counters.hits / K, "misses": counters.misses / K, "resident": counters.resident / K,
                      "h2d_bytes_per_step": counters.h2d_bytes / K, "d2h_bytes_per_step": counters.d2h_bytes / K},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": statistics.mean(host_sess.h2d_bytes),

@@ -15,9 +15,15 @@
 //    sum over rows use a warp transpose-reduction and shared memory;
 //  * P^T (fp16) overwrites the rope columns of the tile; O^T = V^T . P^T on
 //    tcgen05 (M = 128 latent dims per group, N = heads, K = 128 rows);
-//  * the unnormalised partial output and (max, sum) go to a per-split buffer,
-//    and a merge kernel combines the splits with log-sum-exp weights.
+//  * the CTAs of one token form a thread-block cluster: they exchange their
+//    per-head (max, sum) through distributed shared memory, scale their partial
+//    outputs by their log-sum-exp weights into shared memory, and each CTA sums
+//    one slice of the 512 output dims over the cluster and writes it as bf16.
+#include <cooperative_groups.h>
+
 #include "hs_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace hs {
 
@@ -66,20 +72,26 @@ __device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32]) {
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
 attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t* __restrict__ row_ids,
-                 float scale_log2, int n_splits) {
+                 float scale_log2, uint16_t* __restrict__ out, float* __restrict__ lse_out) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* KV = smem + AT_OFF_KV;
   uint8_t* Qs = smem + AT_OFF_Q;
   int32_t* ids = reinterpret_cast<int32_t*>(smem + AT_OFF_MISC);            // [128]
   float* red = reinterpret_cast<float*>(ids + ATTN_ROWS);                    // [4][64]
-  float* mfin = red + 4 * 64;                                                // [64]
-  float* lfin = mfin + 64;                                                   // [64]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(lfin + 64);                    // [1]
+  float* mfin = red + 4 * 64;                                                // [64] this split's max (log2 units)
+  float* lfin = mfin + 64;                                                   // [64] this split's sum
+  float* wmine = lfin + 64;                                                  // [64] weight of this split
+  float* gstat = wmine + 64;                                                 // [64] spare, [64] lse
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gstat + 128);                  // [1]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
   int32_t* s_flag = reinterpret_cast<int32_t*>(tslot + 1);
+  float* Ofull = reinterpret_cast<float*>(KV);                               // [H][512] after PV
 
-  const int split = blockIdx.x, tok = blockIdx.y;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int split = (int)cluster.block_rank();
+  const int n_splits = (int)cluster.num_blocks();
+  const int tok = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = D.n_heads, K = D.topk;
   const uint8_t* kv = D.kv[layer];
@@ -97,59 +109,74 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     if (id >= max_row) { set_status(D.status, HS_ERR_BAD_ID); id = -1; }
     ids[r] = id;
   }
-  // ---- Q: [H, 576] bf16 -> fp16, K-major SW128, one atom column per 64 dims ----
+  // ---- Q loads in flight: [H, 576] bf16, 72 chunks of 8 per head ----
   const uint16_t* qt = q + (size_t)tok * H * QK;
-  for (int c = tid; c < H * 72; c += AT_THREADS) {
-    int h = c / 72, ch = c - h * 72;
-    uint4 v = *reinterpret_cast<const uint4*>(qt + (size_t)h * QK + ch * 8);
-    uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-    *reinterpret_cast<uint4*>(Qs + (ch >> 3) * AT_Q_COL + sw128_chunk(h, ch & 7)) = o;
+  constexpr int QPT = 64 * 72 / AT_THREADS;   // 18 chunks per thread at 64 heads
+  uint4 qv[QPT];
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int c = tid + k * AT_THREADS;
+    qv[k] = c < H * 72 ? __ldg(reinterpret_cast<const uint4*>(qt) + c) : make_uint4(0, 0, 0, 0);
   }
-  __syncthreads();
+  __syncthreads();   // ids ready
 
-  // ---- gather + dequantise 128 rows: warp w takes rows 16w .. 16w+15 ----
-  {
-    const int r0 = warp * 16;
-#pragma unroll 1
-    for (int rb = 0; rb < 16; rb += 4) {
-      uint4 lat[4], sc[4], rp[4];
+  // ---- gather rows: warp w takes rows 16w .. 16w+15 in two batches of 8 ----
+  const int r0 = warp * 16;
+  uint4 lat[8], sc[8], rp[8];
+  auto load_rows = [&](int rb) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int id = ids[r0 + rb + u];
-        lat[u] = make_uint4(0, 0, 0, 0);
-        sc[u] = make_uint4(0, 0, 0, 0);
-        rp[u] = make_uint4(0, 0, 0, 0);
-        if (id >= 0) {
-          const uint8_t* row = kv + (size_t)id * ROW;
-          lat[u] = __ldg(reinterpret_cast<const uint4*>(row + lane * 16));
-          sc[u] = __ldg(reinterpret_cast<const uint4*>(row + LATENT));
-          if (lane < 8) rp[u] = __ldg(reinterpret_cast<const uint4*>(row + LATENT + 16 + lane * 16));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = r0 + rb + u;
-        const int g = lane >> 3;   // latent chunk lane covers dims 16*lane.., group lane/8
-        const float s = __uint_as_float(g == 0 ? sc[u].x : g == 1 ? sc[u].y : g == 2 ? sc[u].z : sc[u].w);
-        uint32_t w[4] = {lat[u].x, lat[u].y, lat[u].z, lat[u].w};
-        uint32_t h[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          h[2 * k] = scale_f16x2(e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffff)), s);
-          h[2 * k + 1] = scale_f16x2(e4m3x2_to_f16x2((uint16_t)(w[k] >> 16)), s);
-        }
-        uint8_t* col = KV + (lane >> 2) * AT_KV_COL;
-        const int chunk = (lane & 3) * 2;
-        *reinterpret_cast<uint4*>(col + sw128_chunk(r, chunk)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(col + sw128_chunk(r, chunk + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-        if (lane < 8) {
-          uint4 o = make_uint4(bf16x2_to_f16x2(rp[u].x), bf16x2_to_f16x2(rp[u].y), bf16x2_to_f16x2(rp[u].z),
-                               bf16x2_to_f16x2(rp[u].w));
-          *reinterpret_cast<uint4*>(KV + 8 * AT_KV_COL + sw128_chunk(r, lane)) = o;
-        }
+    for (int u = 0; u < 8; ++u) {
+      const int id = ids[r0 + rb + u];
+      lat[u] = make_uint4(0, 0, 0, 0);
+      sc[u] = make_uint4(0, 0, 0, 0);
+      rp[u] = make_uint4(0, 0, 0, 0);
+      if (id >= 0) {
+        const uint8_t* row = kv + (size_t)id * ROW;
+        lat[u] = __ldg(reinterpret_cast<const uint4*>(row + lane * 16));
+        sc[u] = __ldg(reinterpret_cast<const uint4*>(row + LATENT));
+        if (lane < 8) rp[u] = __ldg(reinterpret_cast<const uint4*>(row + LATENT + 16 + lane * 16));
       }
     }
+  };
+  auto store_rows = [&](int rb) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int r = r0 + rb + u;
+      const int g = lane >> 3;   // lane's 16 latent dims belong to scale group lane / 8
+      const float s = __uint_as_float(g == 0 ? sc[u].x : g == 1 ? sc[u].y : g == 2 ? sc[u].z : sc[u].w);
+      const uint32_t w[4] = {lat[u].x, lat[u].y, lat[u].z, lat[u].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        h[2 * k] = scale_f16x2(e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffff)), s);
+        h[2 * k + 1] = scale_f16x2(e4m3x2_to_f16x2((uint16_t)(w[k] >> 16)), s);
+      }
+      uint8_t* col = KV + (lane >> 2) * AT_KV_COL;
+      const int chunk = (lane & 3) * 2;
+      *reinterpret_cast<uint4*>(col + sw128_chunk(r, chunk)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(col + sw128_chunk(r, chunk + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+      if (lane < 8) {
+        uint4 o = make_uint4(bf16x2_to_f16x2(rp[u].x), bf16x2_to_f16x2(rp[u].y), bf16x2_to_f16x2(rp[u].z),
+                             bf16x2_to_f16x2(rp[u].w));
+        *reinterpret_cast<uint4*>(KV + 8 * AT_KV_COL + sw128_chunk(r, lane)) = o;
+      }
+    }
+  };
+  load_rows(0);
+  // Q: bf16 -> fp16, K-major SW128, one atom column per 64 dims
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int c = tid + k * AT_THREADS;
+    if (c < H * 72) {
+      const int h = c / 72, ch = c - h * 72;
+      const uint4 v = qv[k];
+      uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+      *reinterpret_cast<uint4*>(Qs + (ch >> 3) * AT_Q_COL + sw128_chunk(h, ch & 7)) = o;
+    }
   }
+  store_rows(0);
+  load_rows(8);
+  store_rows(8);
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -201,10 +228,7 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     red[quad * 64 + hh * 32 + lane] = warp_transpose_reduce32<true>(t);
   }
   __syncthreads();
-  if (tid < H) {
-    float m = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
-    mfin[tid] = m;
-  }
+  if (tid < H) mfin[tid] = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
   __syncthreads();
   if (active) {
     float t[32];
@@ -251,13 +275,27 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     }
     umma_commit(smem_u32(bar));
   }
+  // (max, sum) of this split are published to the cluster while the PV product runs
+  cluster.sync();
+  // ---- cluster-wide log-sum-exp weight of this split, per head ----
+  if (tid < H) {
+    float M = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, cluster.map_shared_rank(mfin, s)[tid]);
+    float L = 0.f;
+    for (int s = 0; s < n_splits; ++s) {
+      const float ms = cluster.map_shared_rank(mfin, s)[tid];
+      if (ms != -INFINITY) L += exp2f(ms - M) * cluster.map_shared_rank(lfin, s)[tid];
+    }
+    const float mine = mfin[tid];
+    wmine[tid] = (L > 0.f && mine != -INFINITY) ? exp2f(mine - M) / L : 0.f;
+    gstat[64 + tid] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
   if (!mbar_wait(smem_u32(bar), 1, D.status)) *s_flag = 1;
   tc_fence_after();
+  __syncthreads();
 
-  // ---- write the unnormalised partial O[head][dim] and (max, sum) ----
-  const size_t part = (size_t)tok * MAX_SPLITS + split;
-  if (active && !*s_flag) {
-    float* op = D.o_part + part * (size_t)H * 512;
+  // ---- weighted partial O[head][dim] (fp32) into this CTA's shared memory ----
+  if (active) {
     for (int g = 0; g < 4; ++g) {
       const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(64 + g * 64 + hh * 32);
       const int dim = g * 128 + quad * 32 + lane;
@@ -266,76 +304,67 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
         tmem_ld32(ta, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) op[(size_t)(hh * 32 + i) * 512 + dim] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) Ofull[(hh * 32 + i) * 512 + dim] = __uint_as_float(r[i]) * wmine[hh * 32 + i];
       } else {
         uint32_t r[16];
         tmem_ld16(ta, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) op[(size_t)(hh * 32 + i) * 512 + dim] = __uint_as_float(r[i]);
+        for (int i = 0; i < 16; ++i) Ofull[(hh * 32 + i) * 512 + dim] = __uint_as_float(r[i]) * wmine[hh * 32 + i];
       }
     }
   }
-  if (tid < H) D.ml_part[part * H + tid] = make_float2(mfin[tid], lfin[tid]);
   tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 512);
-}
-
-// Combine the splits of every (token, head): log-sum-exp weights, bf16 output.
-__global__ void __launch_bounds__(128)
-merge_kernel(Dev D, int n_splits, uint16_t* __restrict__ out, float* __restrict__ lse) {
-  const int tok = blockIdx.x, h = blockIdx.y, H = D.n_heads;
-  __shared__ float w[MAX_SPLITS];
-  __shared__ float s_inv, s_lse;
-  const size_t base = (size_t)tok * MAX_SPLITS;
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, D.ml_part[(base + s) * H + h].x);
-    float L = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-      float2 ml = D.ml_part[(base + s) * H + h];
-      float ws = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-      w[s] = ws;
-      L += ws * ml.y;
+  cluster.sync();
+  // ---- this CTA sums one slice of the 512 dims over the cluster and writes bf16 ----
+  {
+    const int slice = ((512 / n_splits) + 3) & ~3;
+    const int d_lo = min(512, split * slice), d_hi = min(512, d_lo + slice);
+    const int per_head = (d_hi - d_lo) / 4;          // float4s per head in the slice
+    for (int e = tid; e < H * per_head; e += AT_THREADS) {
+      const int h = e / per_head, d = d_lo + (e - h * per_head) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < n_splits; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(Ofull, s) + h * 512 + d);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(out + ((size_t)tok * H + h) * 512 + d) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
     }
-    s_inv = L > 0.f ? 1.f / L : 0.f;
-    s_lse = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    if (split == 0 && lse_out && tid < H) lse_out[(size_t)tok * H + tid] = gstat[64 + tid];
   }
-  __syncthreads();
-  const int d0 = threadIdx.x * 4;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < n_splits; ++s) {
-    const float ws = w[s];
-    if (ws == 0.f) continue;
-    const float4 v = *reinterpret_cast<const float4*>(D.o_part + ((base + s) * H + h) * 512 + d0);
-    acc[0] += ws * v.x;
-    acc[1] += ws * v.y;
-    acc[2] += ws * v.z;
-    acc[3] += ws * v.w;
-  }
-  const float inv = s_inv;
-  __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-  __nv_bfloat162 b = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-  uint2 o = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
-  *reinterpret_cast<uint2*>(out + ((size_t)tok * H + h) * 512 + d0) = o;
-  if (lse && threadIdx.x == 0) lse[(size_t)tok * H + h] = s_lse;
+  cluster.sync();   // peers read this CTA's shared memory until here
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows, float sm_scale,
                            uint16_t* d_out, float* d_lse, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return HS_ERR_CUDA;
     attr = true;
   }
   const int n_splits = (p->cfg.topk + ATTN_ROWS - 1) / ATTN_ROWS;
-  attention_kernel<<<dim3(n_splits, n), AT_THREADS, AT_SMEM, st>>>(p->d, layer, d_q, d_rows, sm_scale * LOG2E,
-                                                                  n_splits);
-  if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
-  merge_kernel<<<dim3(n, p->cfg.n_heads), 128, 0, st>>>(p->d, n_splits, d_out, d_lse);
-  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(n_splits, n, 1);
+  lc.blockDim = dim3(AT_THREADS, 1, 1);
+  lc.dynamicSmemBytes = AT_SMEM;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = n_splits;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, attention_kernel, p->d, layer, d_q, d_rows, sm_scale * LOG2E, d_out, d_lse) !=
+      cudaSuccess)
+    return HS_ERR_CUDA;
+  return HS_OK;
 }
 
 }  // namespace hs

@@ -8,7 +8,9 @@
 // Scoring kernel (one persistent CTA per SM):
 //  * work item = (request segment, 128-key tile); the T <= 4 query tokens of a
 //    request share each key tile, so the keys are read from HBM once per request;
-//  * key pages (64 x 128 B) arrive by bulk copy (TMA unit) into a 6-stage ring;
+//  * key pages (64 x 128 B) arrive by bulk copy (TMA unit) into a 4-stage ring
+//    filled by a producer warp; converter warps, an MMA warp and epilogue warps
+//    work on consecutive tiles at once (double-buffered A tiles and accumulators);
 //  * int8 keys and queries are widened to fp16 (exact for |x| <= 128) in the
 //    128-byte-swizzled K-major layout and contracted on the tensor cores with
 //    tcgen05.mma kind::f16 (M = 128 keys, N = T * H_i, K = 128); the products
@@ -16,10 +18,12 @@
 //  * the epilogue reads the accumulator from tensor memory, applies ReLU and
 //    the head weights in integer arithmetic and writes int64 scores.
 //
-// Select kernel (one 8-CTA cluster per query token): exact radix select of the
-// K-th largest score using shared-memory histograms merged through distributed
-// shared memory, then an ordered compaction that emits the selected token ids
-// in ascending order with ties broken toward the lower token index.
+// Select kernel (one 8- or 16-CTA cluster per query token): a shared-memory
+// histogram of a monotone bucket of each (score, token) key, merged through
+// distributed shared memory, finds the bucket of the K-th largest; the few keys
+// in that bucket are sorted by the cluster leader to give the exact threshold
+// key (a multi-level histogram refinement takes over when a bucket is crowded);
+// each CTA then emits its selected tokens in ascending order at its offset.
 #include <cooperative_groups.h>
 
 #include "hs_internal.cuh"
@@ -31,19 +35,26 @@ namespace hs {
 // ----------------------------------------------------------------------------------
 // Scoring kernel
 // ----------------------------------------------------------------------------------
-constexpr int IX_THREADS = 256;
-constexpr int IX_STAGES = 6;
+// Warp roles (320 threads):
+//   warps 0-3  epilogue: TMEM accumulator -> ReLU, head weights, int64 scores
+//   warps 4-7  convert: raw int8 key tile -> fp16 A tile; queries -> fp16 B operand
+//   warp 8     producer: bulk copies of key pages into a 4-stage ring
+//   warp 9     MMA issuer: tcgen05.mma into one of two TMEM accumulators
+constexpr int IX_THREADS = 320;
+constexpr int IX_STAGES = 4;
 constexpr int IX_TILE = 128;
 constexpr int IX_RAW = IX_TILE * IDX_DIM;              // 16 KB int8 per tile
 constexpr int IX_A_COL = IX_TILE * 128;                // one 64-dim fp16 atom column, 16 KB
+constexpr int IX_A = 2 * IX_A_COL;                     // 32 KB per A tile
 constexpr int IX_B_COL = 256 * 128;                    // B atom column for up to N = 256 rows
 constexpr int IX_MAX_SEG = 1024;
-constexpr int IX_OFF_A = 0;
-constexpr int IX_OFF_B = IX_OFF_A + 2 * IX_A_COL;      // 32 KB
-constexpr int IX_OFF_RAW = IX_OFF_B + 2 * IX_B_COL;    // 96 KB
-constexpr int IX_OFF_BAR = IX_OFF_RAW + IX_STAGES * IX_RAW;
-constexpr int IX_OFF_SEG = IX_OFF_BAR + 128;
+constexpr int IX_OFF_A = 0;                            // 2 A tiles
+constexpr int IX_OFF_B = IX_OFF_A + 2 * IX_A;          // 64 KB
+constexpr int IX_OFF_RAW = IX_OFF_B + 2 * IX_B_COL;    // 128 KB
+constexpr int IX_OFF_BAR = IX_OFF_RAW + IX_STAGES * IX_RAW;   // 192 KB
+constexpr int IX_OFF_SEG = IX_OFF_BAR + 256;
 constexpr int IX_SMEM = IX_OFF_SEG + IX_MAX_SEG * 16 + 4 * 64 * 4 + 2 * IX_MAX_SEG * 4 + 1024;
+constexpr int IX_TMEM_COLS = 512;                      // two accumulators of up to 256 columns
 
 struct IxSeg {
   int32_t first;     // first token of the segment
@@ -70,17 +81,33 @@ __device__ __forceinline__ void i8x16_to_f16(uint4 v, uint4& c0, uint4& c1) {
   c1 = make_uint4(c.x, c.y, d.x, d.y);
 }
 
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __global__ void __launch_bounds__(IX_THREADS, 1)
 indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, const int32_t* __restrict__ limit_of,
-               const int8_t* __restrict__ qg, const int8_t* __restrict__ wg, int64_t* __restrict__ scores) {
+               const int8_t* __restrict__ qg, const int8_t* __restrict__ wg, int64_t* __restrict__ scores,
+               int ld) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + IX_OFF_BAR);     // [0..S) full, [S] mma
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + IX_OFF_BAR + 8 * (IX_STAGES + 1));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + IX_OFF_BAR);
+  uint64_t* raw_full = bars;                      // [4]
+  uint64_t* raw_empty = bars + 4;                 // [4]
+  uint64_t* a_full = bars + 8;                    // [2]
+  uint64_t* a_empty = bars + 10;                  // [2]
+  uint64_t* t_full = bars + 12;                   // [2]
+  uint64_t* t_empty = bars + 14;                  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   int32_t* s_nseg = reinterpret_cast<int32_t*>(tmem_slot + 1);
-  int32_t* s_flag = s_nseg + 1;
+  int32_t* s_dead = s_nseg + 1;
+  int32_t* s_issued = s_nseg + 2;
+  int32_t* s_consumed = s_nseg + 3;
   IxSeg* segs = reinterpret_cast<IxSeg*>(smem + IX_OFF_SEG);
-  int32_t* s_w = reinterpret_cast<int32_t*>(smem + IX_OFF_SEG + IX_MAX_SEG * 16);   // [4][64]
+  int32_t* s_w = reinterpret_cast<int32_t*>(smem + IX_OFF_SEG + IX_MAX_SEG * 16);   // [4][64], epilogue-owned
   int32_t* s_req = s_w + 4 * 64;                                                      // [n_tok]
   int32_t* s_lim = s_req + IX_MAX_SEG;                                                // [n_tok]
 
@@ -91,7 +118,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   // ---- request segments of the batch (tokens of one request are contiguous) ----
   for (int t = tid; t < n_tok; t += IX_THREADS) {
     int r = req_of[t], lim = limit_of[t];
-    if (r < 0 || r >= D.max_requests || lim < 0 || lim > D.max_ctx) {
+    if (r < 0 || r >= D.max_requests || lim < 0 || lim > D.max_ctx || lim > ld) {
       set_status(D.status, HS_ERR_BAD_ID);
       r = 0;
       lim = 0;
@@ -118,11 +145,13 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
       segs[i].tile_end = tiles;
     }
     *s_nseg = ns;
-    for (int st = 0; st <= IX_STAGES; ++st) mbar_init(smem_u32(&bars[st]), 1);
+    for (int b = 0; b < 16; ++b) mbar_init(smem_u32(&bars[b]), 1);
     fence_mbar_init();
-    *s_flag = 0;
+    *s_dead = 0;
+    *s_issued = 0;
+    *s_consumed = 0;
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 256);
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), IX_TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -139,172 +168,210 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
     }
     return lo;
   };
-  // issue the bulk copies of the (up to two) key pages of local item i into its stage
-  auto issue = [&](int i) {
-    int item = (int)blockIdx.x + i * (int)gridDim.x;
-    int sg = seg_of(item);
-    int tile = item - (sg ? segs[sg - 1].tile_end : 0);
-    int r = s_req[segs[sg].first];
-    int stage = i % IX_STAGES;
-    uint32_t bar = smem_u32(&bars[stage]);
-    uint32_t dst = smem_u32(smem + IX_OFF_RAW + stage * IX_RAW);
-    int npg = ((tile * IX_TILE + PAGE) < segs[sg].maxlim) ? 2 : 1;
-    int ip[2] = {-1, -1};
-    uint32_t bytes = 0;
-    for (int k = 0; k < npg; ++k) {
-      int v = D.idx_bt[(size_t)r * D.max_pages + tile * 2 + k];
-      if (v < 0 || v >= D.num_idx_pages) {
-        set_status(D.status, HS_ERR_BAD_ID);
-        continue;
-      }
-      ip[k] = v;
-      bytes += IDX_PAGE_BYTES;
-    }
-    mbar_expect_tx(bar, bytes);
-    for (int k = 0; k < 2; ++k)
-      if (ip[k] >= 0) bulk_g2s(dst + k * IDX_PAGE_BYTES, keys + (size_t)ip[k] * IDX_PAGE_BYTES, IDX_PAGE_BYTES, bar);
-  };
+  auto item_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
-  int issued = 0;   // meaningful in thread 0 only
-  if (tid == 0) {
-    for (int i = 0; i < min(n_local, IX_STAGES); ++i) issue(i);
-    issued = min(n_local, IX_STAGES);
-  }
-
-  int cur_seg = -1;
-  bool dead = false;
-  int died_at = 0;
-  for (int i = 0; i < n_local && !dead; ++i) {
-    const int item = (int)blockIdx.x + i * (int)gridDim.x;
-    const int sg = seg_of(item);
-    const IxSeg S = segs[sg];
-    const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
-    const int key0 = tile * IX_TILE;
-    const int N = ((S.ntok * Hi) + 15) & ~15;
-
-    if (sg != cur_seg) {
-      // load the segment's queries as the B operand: row n = j * Hi + h, K-major SW128
-      uint8_t* B = smem + IX_OFF_B;
-      const int rows = N;
-      for (int c = tid; c < rows * 8; c += IX_THREADS) {
-        int row = c >> 3, ch16 = c & 7;            // 8 chunks of 16 int8 per 128-dim row
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < S.ntok * Hi) {
-          int j = row / Hi, h = row - j * Hi;
-          v = *reinterpret_cast<const uint4*>(qg + ((size_t)(S.first + j) * Hi + h) * IDX_DIM + ch16 * 16);
+  if (warp == 8) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      for (int i = 0; i < n_local; ++i) {
+        const int rs = i % IX_STAGES;
+        if (i >= IX_STAGES && !mbar_wait(smem_u32(&raw_empty[rs]), ((i / IX_STAGES) - 1) & 1, D.status)) {
+          *s_dead = 1;
+          break;
         }
+        if (*(volatile int32_t*)s_dead) break;
+        const int item = item_of(i);
+        const int sg = seg_of(item);
+        const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
+        const int r = s_req[segs[sg].first];
+        const uint32_t bar = smem_u32(&raw_full[rs]);
+        const uint32_t dst = smem_u32(smem + IX_OFF_RAW + rs * IX_RAW);
+        const int npg = ((tile * IX_TILE + PAGE) < segs[sg].maxlim) ? 2 : 1;
+        int ip[2] = {-1, -1};
+        uint32_t bytes = 0;
+        for (int k = 0; k < npg; ++k) {
+          int v = D.idx_bt[(size_t)r * D.max_pages + tile * 2 + k];
+          if (v < 0 || v >= D.num_idx_pages) { set_status(D.status, HS_ERR_BAD_ID); continue; }
+          ip[k] = v;
+          bytes += IDX_PAGE_BYTES;
+        }
+        mbar_expect_tx(bar, bytes);
+        for (int k = 0; k < 2; ++k)
+          if (ip[k] >= 0) bulk_g2s(dst + k * IDX_PAGE_BYTES, keys + (size_t)ip[k] * IDX_PAGE_BYTES, IDX_PAGE_BYTES, bar);
+        *s_issued = i + 1;
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      for (int i = 0; i < n_local; ++i) {
+        const int ab = i & 1;
+        if (!mbar_wait(smem_u32(&a_full[ab]), (i >> 1) & 1, D.status)) { *s_dead = 1; break; }
+        if (i >= 2 && !mbar_wait(smem_u32(&t_empty[ab]), ((i >> 1) - 1) & 1, D.status)) { *s_dead = 1; break; }
+        if (*(volatile int32_t*)s_dead) break;
+        tc_fence_after();
+        const IxSeg S = segs[seg_of(item_of(i))];
+        const int N = ((S.ntok * Hi) + 15) & ~15;
+        const uint32_t idesc = idesc_f16(128, N, false, false);
+        const uint32_t a0 = smem_u32(smem + IX_OFF_A + ab * IX_A), b0 = smem_u32(smem + IX_OFF_B);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * IX_A_COL + (kk & 3) * 32, 16, 1024);
+          uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * IX_B_COL + (kk & 3) * 32, 16, 1024);
+          umma_f16(tmem + ab * 256, ad, bd, idesc, kk > 0);
+        }
+        umma_commit(smem_u32(&a_empty[ab]));
+        umma_commit(smem_u32(&t_full[ab]));
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------ converters ------------------------------
+    const int ct = tid - 128;
+    int cur_seg = -1;
+    for (int i = 0; i < n_local; ++i) {
+      const int item = item_of(i);
+      const int sg = seg_of(item);
+      const IxSeg S = segs[sg];
+      const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
+      const int key0 = tile * IX_TILE;
+      bool ok = true;
+      if (sg != cur_seg) {
+        // every MMA reading the previous queries has completed before they are replaced
+        if (i > 0) ok = mbar_wait(smem_u32(&a_empty[(i - 1) & 1]), ((i - 1) >> 1) & 1, D.status);
+        uint8_t* B = smem + IX_OFF_B;
+        const int N = ((S.ntok * Hi) + 15) & ~15;
+        for (int c = ct; c < N * 8; c += 128) {
+          const int row = c >> 3, ch16 = c & 7;       // 8 chunks of 16 int8 per 128-dim row
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < S.ntok * Hi) {
+            const int j = row / Hi, h = row - j * Hi;
+            v = *reinterpret_cast<const uint4*>(qg + ((size_t)(S.first + j) * Hi + h) * IDX_DIM + ch16 * 16);
+          }
+          uint4 c0, c1;
+          i8x16_to_f16(v, c0, c1);
+          const int dim0 = ch16 * 16;
+          uint8_t* base = B + (dim0 >> 6) * IX_B_COL;
+          const int chunk = (dim0 & 63) >> 3;
+          *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk)) = c0;
+          *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk + 1)) = c1;
+        }
+        cur_seg = sg;
+      }
+      const int rs = i % IX_STAGES, ab = i & 1;
+      if (ok) ok = mbar_wait(smem_u32(&raw_full[rs]), (i / IX_STAGES) & 1, D.status);
+      if (ok && i >= 2) ok = mbar_wait(smem_u32(&a_empty[ab]), ((i >> 1) - 1) & 1, D.status);
+      if (!ok) *s_dead = 1;
+      const uint8_t* raw = smem + IX_OFF_RAW + rs * IX_RAW;
+      uint8_t* A = smem + IX_OFF_A + ab * IX_A;
+      for (int c = ct; c < IX_TILE * 8; c += 128) {
+        const int row = c >> 3, ch16 = c & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (key0 + row < S.maxlim) v = *reinterpret_cast<const uint4*>(raw + row * IDX_DIM + ch16 * 16);
         uint4 c0, c1;
         i8x16_to_f16(v, c0, c1);
-        int dim0 = ch16 * 16;                       // 16 dims -> fp16 chunks (dim0/8, dim0/8+1)
-        int col = dim0 >> 6;                        // atom column
-        int chunk = (dim0 & 63) >> 3;
-        uint8_t* base = B + col * IX_B_COL;
+        const int dim0 = ch16 * 16;
+        uint8_t* base = A + (dim0 >> 6) * IX_A_COL;
+        const int chunk = (dim0 & 63) >> 3;
         *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk)) = c0;
         *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk + 1)) = c1;
       }
-      for (int c = tid; c < 4 * 64; c += IX_THREADS) {
-        int j = c >> 6, h = c & 63;
-        int w = 0;
-        if (j < S.ntok && h < Hi) {
-          w = wg[(size_t)(S.first + j) * Hi + h];
-          if (w < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); w = 0; }
+      fence_proxy_async();
+      named_sync(1, 128);
+      if (ct == 0) {
+        *s_consumed = i + 1;
+        mbar_arrive(smem_u32(&raw_empty[rs]));
+        mbar_arrive(smem_u32(&a_full[ab]));
+      }
+      if (*(volatile int32_t*)s_dead) break;
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    int cur_seg = -1;
+    for (int i = 0; i < n_local; ++i) {
+      const int item = item_of(i);
+      const int sg = seg_of(item);
+      const IxSeg S = segs[sg];
+      const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
+      const int key = tile * IX_TILE + warp * 32 + lane;
+      if (sg != cur_seg) {
+        named_sync(2, 128);
+        for (int c = tid; c < 4 * 64; c += 128) {
+          const int j = c >> 6, h = c & 63;
+          int w = 0;
+          if (j < S.ntok && h < Hi) {
+            w = wg[(size_t)(S.first + j) * Hi + h];
+            if (w < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); w = 0; }
+          }
+          s_w[c] = w;
         }
-        s_w[c] = w;
+        named_sync(2, 128);
+        cur_seg = sg;
       }
-      cur_seg = sg;
-    }
-
-    // ---- wait for the key tile, widen to fp16 (A operand: M = keys, K-major) ----
-    const int stage = i % IX_STAGES;
-    if (!mbar_wait(smem_u32(&bars[stage]), (i / IX_STAGES) & 1, D.status)) *s_flag = 1;
-    const uint8_t* raw = smem + IX_OFF_RAW + stage * IX_RAW;
-    uint8_t* A = smem + IX_OFF_A;
-    for (int c = tid; c < IX_TILE * 8; c += IX_THREADS) {
-      int row = c >> 3, ch16 = c & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (key0 + row < S.maxlim) v = *reinterpret_cast<const uint4*>(raw + row * IDX_DIM + ch16 * 16);
-      uint4 c0, c1;
-      i8x16_to_f16(v, c0, c1);
-      int dim0 = ch16 * 16;
-      uint8_t* base = A + (dim0 >> 6) * IX_A_COL;
-      int chunk = (dim0 & 63) >> 3;
-      *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk)) = c0;
-      *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk + 1)) = c1;
-    }
-    fence_proxy_async();
-    __syncthreads();
-    if (*s_flag) { dead = true; died_at = i; break; }
-    if (tid == 0) {
-      if (i + IX_STAGES < n_local) {
-        issue(i + IX_STAGES);
-        issued = i + IX_STAGES + 1;
-      }
+      const int ab = i & 1;
+      if (!mbar_wait(smem_u32(&t_full[ab]), (i >> 1) & 1, D.status)) { *s_dead = 1; break; }
       tc_fence_after();
-      const uint32_t idesc = idesc_f16(128, N, false, false);
-      const uint32_t a0 = smem_u32(A), b0 = smem_u32(smem + IX_OFF_B);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * IX_A_COL + (kk & 3) * 32, 16, 1024);
-        uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * IX_B_COL + (kk & 3) * 32, 16, 1024);
-        umma_f16(tmem, ad, bd, idesc, kk > 0);
-      }
-      umma_commit(smem_u32(&bars[IX_STAGES]));
-    }
-    if (!mbar_wait(smem_u32(&bars[IX_STAGES]), i & 1, D.status)) *s_flag = 1;
-    tc_fence_after();
-
-    // ---- epilogue: warp w reads TMEM lanes 32*(w%4).., tokens j = w/4, w/4 + 2 ----
-    {
-      const int quad = warp & 3;
-      const int key = key0 + quad * 32 + lane;
-      const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-      for (int j = warp >> 2; j < 4; j += 2) {
-        if (j >= S.ntok) break;      // warp-uniform
+      for (int j = 0; j < S.ntok; ++j) {
         const int lim = s_lim[S.first + j];
         long long acc = 0;
         for (int h0 = 0; h0 < Hi; h0 += 16) {
           uint32_t r[16];
-          tmem_ld16(lane_addr + (uint32_t)(j * Hi + h0), r);
+          tmem_ld16(lane_base + (uint32_t)(ab * 256 + j * Hi + h0), r);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            int v = __float2int_rn(__uint_as_float(r[k]));
-            v = max(v, 0);
+            const int v = max(__float2int_rn(__uint_as_float(r[k])), 0);
             acc += (long long)v * s_w[j * 64 + h0 + k];
           }
         }
-        if (key < lim) scores[(size_t)(S.first + j) * D.max_ctx + key] = acc;
+        if (key < lim) scores[(size_t)(S.first + j) * ld + key] = acc;
       }
+      tc_fence_before();
+      named_sync(2, 128);
+      if (tid == 0) mbar_arrive(smem_u32(&t_empty[ab]));
+      if (*(volatile int32_t*)s_dead) break;
     }
-    tc_fence_before();
-    __syncthreads();
-    if (*s_flag) { dead = true; died_at = i + 1; }
   }
   __syncthreads();
-  if (dead && tid == 0) {
+  if (*s_dead && tid == 8 * 32) {
     // drain bulk copies still in flight before the CTA's shared memory goes away
-    for (int k = died_at; k < issued; ++k) mbar_wait(smem_u32(&bars[k % IX_STAGES]), (k / IX_STAGES) & 1, D.status);
+    for (int k = *s_consumed; k < *s_issued; ++k)
+      mbar_wait(smem_u32(&raw_full[k % IX_STAGES]), (k / IX_STAGES) & 1, D.status);
   }
+  tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, IX_TMEM_COLS);
 }
 
 // ----------------------------------------------------------------------------------
 // Select kernel
 // ----------------------------------------------------------------------------------
-constexpr int SEL_CL = 8;
+// Each score s of token index t is made unique and order-preserving as the key
+//   key = s * 2^21 + (2^21 - 1 - t)          (s >= 0, t < 2^21)
+// so the top K by (score desc, token asc) are exactly the K largest keys, and the
+// K-th largest key tau selects them with the single test key >= tau.
 constexpr int SEL_THREADS = 512;
 constexpr int SEL_BINS = 4096;
-constexpr int SEL_SLICE = SEL_BINS / SEL_CL;
-constexpr int SEL_CACHE = 24576;                       // scores cached in shared memory per CTA
-constexpr int SEL_SMEM = SEL_CACHE * 8 + 1024;
+constexpr int SEL_CACHE = 20480;                       // keys cached in shared memory per CTA
+constexpr int SEL_CAND = 2048;                         // candidates per CTA on the fast path
+constexpr int SEL_LEAD = 4096;                         // candidates the cluster leader sorts
+constexpr int SEL_SMEM = SEL_CACHE * 8 + SEL_LEAD * 8 + 1024;
+constexpr unsigned long long IDX_MASK = (1ull << 21) - 1;
 
-// monotone level-1 bucket: exact below 64, then 64 buckets per octave
-__device__ __forceinline__ int bucket1(long long v) {
-  if (v < 64) return v < 0 ? 0 : (int)v;
-  int e = 63 - __clzll(v);
+// monotone level-0 bucket of a key: exact below 64, then 64 buckets per octave
+__device__ __forceinline__ int bucket1(unsigned long long v) {
+  if (v < 64) return (int)v;
+  int e = 63 - __clzll((long long)v);
   int m = (int)((v >> (e - 6)) & 63);
   return 64 + (e - 6) * 64 + m;
+}
+
+// warp-aggregated shared-memory histogram increment
+__device__ __forceinline__ void hist_add(uint32_t* hist, int bin) {
+  const unsigned act = __activemask();
+  const unsigned peers = __match_any_sync(act, bin);
+  if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
 }
 
 __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
@@ -333,164 +400,199 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
   return res;
 }
 
-__global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS, 1)
+// descending bitonic sort of n (power of two) keys
+__device__ void bitonic_desc(unsigned long long* a, int n) {
+  for (int k = 2; k <= n; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int p = i ^ j;
+        if (p > i) {
+          unsigned long long x = a[i], y = a[p];
+          bool desc = (i & k) == 0;
+          if ((x < y) == desc) { a[i] = y; a[p] = x; }
+        }
+      }
+      __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(SEL_THREADS, 1)
 select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of,
               int32_t* __restrict__ topk) {
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
-  const int tok = blockIdx.x / SEL_CL;
+  const int CL = (int)cluster.num_blocks();
+  const int slice = SEL_BINS / CL;
+  const int tok = blockIdx.x / CL;
   const int K = D.topk;
-  __shared__ uint32_t hist[SEL_BINS];
-  __shared__ uint32_t tot[SEL_SLICE];
+  const int tid = threadIdx.x;
+  __shared__ uint32_t hist[SEL_BINS];      // level histograms; later the candidate list
+  __shared__ uint32_t tot[SEL_BINS / 8];
   __shared__ int warp_tot[32];
-  __shared__ int s_sum;
+  __shared__ int s_sum, s_bin, s_ncand, s_over, s_nsel;
   __shared__ long long s_above;
-  __shared__ int s_bin;
-  __shared__ int cnt[2];
+  __shared__ unsigned long long s_tau;
   extern __shared__ __align__(16) uint8_t sel_dyn[];
-  long long* cache = reinterpret_cast<long long*>(sel_dyn);
+  unsigned long long* cache = reinterpret_cast<unsigned long long*>(sel_dyn);            // [SEL_CACHE]
+  unsigned long long* lead = cache + SEL_CACHE;                                           // [SEL_LEAD]
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(hist);                 // [SEL_CAND]
+  int32_t* elist = reinterpret_cast<int32_t*>(lead);                                      // [K] after tau
 
   int n = limit_of[tok];
   n = max(0, min(n, D.max_ctx));
   int32_t* out = topk + (size_t)tok * K;
   if (n <= K) {           // every earlier token is selected (uniform across the cluster)
     if (crank == 0)
-      for (int i = threadIdx.x; i < K; i += blockDim.x) out[i] = i < n ? i : -1;
+      for (int i = tid; i < K; i += blockDim.x) out[i] = i < n ? i : -1;
     return;
   }
   const long long* s = reinterpret_cast<const long long*>(scores) + (size_t)tok * ld;
-  const int per = (n + SEL_CL - 1) / SEL_CL;
+  const int per = (n + CL - 1) / CL;
   const int lo = crank * per, hi = min(n, lo + per);
   const int cnt_local = max(0, hi - lo);
   const bool cached = per <= SEL_CACHE;
+  auto key_at = [&](int i) -> unsigned long long {
+    if (cached) return cache[i];
+    long long v = s[lo + i];
+    return ((unsigned long long)max(v, 0ll) << 21) | (IDX_MASK - (unsigned long long)(lo + i));
+  };
 
+  // ---- level 0: histogram of bucket1(key); find the bucket of the K-th largest ----
+  for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = 0;
+  if (tid == 0) { s_ncand = 0; s_over = 0; s_bin = 0; s_above = 0; }
+  __syncthreads();
+  for (int i = tid; i < cnt_local; i += blockDim.x) {
+    long long v = s[lo + i];
+    if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
+    const unsigned long long k = ((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + i));
+    if (cached) cache[i] = k;
+    hist_add(hist, bucket1(k));
+  }
   int need = K;
-  int level = 0;
-  long long base = 0, width = 0;   // level >= 1: value range [base, base + width)
-  int shift = 0;
-  for (;; ++level) {
-    for (int b = threadIdx.x; b < SEL_BINS; b += blockDim.x) hist[b] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < cnt_local; i += blockDim.x) {
-      long long v;
-      if (level == 0) {
-        v = s[lo + i];
-        if (cached) cache[i] = v;
-        atomicAdd(&hist[bucket1(v)], 1u);
-      } else {
-        v = cached ? cache[i] : s[lo + i];
-        if (v >= base && v - base < width) atomicAdd(&hist[(int)((v - base) >> shift)], 1u);
-      }
-    }
+  auto cluster_find = [&](void) {
     cluster.sync();
-    // reduce my slice of bins over the cluster
-    for (int b = threadIdx.x; b < SEL_SLICE; b += blockDim.x) {
+    for (int b = tid; b < slice; b += blockDim.x) {
       uint32_t a = 0;
-#pragma unroll
-      for (int r = 0; r < SEL_CL; ++r) a += cluster.map_shared_rank(hist, r)[crank * SEL_SLICE + b];
+      for (int r = 0; r < CL; ++r) a += cluster.map_shared_rank(hist, r)[crank * slice + b];
       tot[b] = a;
     }
     cluster.sync();
-    for (int b = threadIdx.x; b < SEL_BINS; b += blockDim.x)
-      hist[b] = cluster.map_shared_rank(tot, b / SEL_SLICE)[b % SEL_SLICE];
+    for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = cluster.map_shared_rank(tot, b / slice)[b % slice];
+    if (tid == 0) { s_bin = 0; s_above = 0; }
     __syncthreads();
-    // find the bin holding the need-th largest value, scanning from the top bin
-    if (threadIdx.x == 0) { s_bin = 0; s_above = 0; }
+    const int per_t = SEL_BINS / SEL_THREADS;     // 8 bins per thread, thread 0 = top bins
+    int local = 0;
+    for (int k = 0; k < per_t; ++k) local += hist[SEL_BINS - 1 - (tid * per_t + k)];
+    int before = block_excl_scan(local, warp_tot, nullptr);
+    if (before < need && need <= before + local) {
+      int cum = before;
+      for (int k = 0; k < per_t; ++k) {
+        int b = SEL_BINS - 1 - (tid * per_t + k);
+        if (cum + (int)hist[b] >= need) { s_bin = b; s_above = cum; break; }
+        cum += hist[b];
+      }
+    }
     __syncthreads();
-    {
-      const int per_t = SEL_BINS / SEL_THREADS;     // 8 bins per thread, thread 0 = top bins
-      int local = 0;
-      for (int k = 0; k < per_t; ++k) local += hist[SEL_BINS - 1 - (threadIdx.x * per_t + k)];
-      int before = block_excl_scan(local, warp_tot, nullptr);
-      if (before < need && need <= before + local) {
-        int cum = before;
-        for (int k = 0; k < per_t; ++k) {
-          int b = SEL_BINS - 1 - (threadIdx.x * per_t + k);
-          if (cum + (int)hist[b] >= need) { s_bin = b; s_above = cum; break; }
-          cum += hist[b];
-        }
-      }
-      __syncthreads();
-    }
-    const int B = s_bin;
-    need -= (int)s_above;
-    if (level == 0) {
-      if (B < 64) { base = B; width = 1; }
-      else {
-        int e = (B - 64) / 64 + 6, m = (B - 64) % 64;
-        base = (1ll << e) + ((long long)m << (e - 6));
-        width = 1ll << (e - 6);
-      }
-    } else {
-      base += (long long)B << shift;
-      width = 1ll << shift;
-    }
-    if (width == 1) break;
-    int lw = 63 - __clzll(width);
-    shift = lw > 12 ? lw - 12 : 0;
-  }
-  const long long tau = base;   // the K-th largest score; `need` of its ties are taken
+  };
+  cluster_find();
+  const int B0 = s_bin;
+  need -= (int)s_above;
+  cluster.sync();           // every CTA is done reading peers' tot[] / hist[] of level 0
 
-  // ---- counts per CTA, prefix over the cluster (CTA ranks own ascending ranges) ----
-  int gt = 0, eq = 0;
-  for (int i = threadIdx.x; i < cnt_local; i += blockDim.x) {
-    long long v = cached ? cache[i] : s[lo + i];
-    gt += v > tau;
-    eq += v == tau;
-  }
-  gt = __reduce_add_sync(0xffffffffu, gt);
-  eq = __reduce_add_sync(0xffffffffu, eq);
-  if (threadIdx.x == 0) { cnt[0] = 0; cnt[1] = 0; }
+  // ---- fast path: collect the keys of bucket B0, the leader sorts them ----
+  if (tid == 0) s_ncand = 0;
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) { atomicAdd(&cnt[0], gt); atomicAdd(&cnt[1], eq); }
-  cluster.sync();
-  int out_off = 0, eq_before = 0;
-  for (int r = 0; r < crank; ++r) {
-    int* pc = cluster.map_shared_rank(cnt, r);
-    int g = pc[0], e = pc[1];
-    int take = max(0, min(e, need - eq_before));
-    out_off += g + take;
-    eq_before += e;
+  for (int i = tid; i < cnt_local; i += blockDim.x) {
+    const unsigned long long k = key_at(i);
+    if (bucket1(k) == B0) {
+      int at = atomicAdd(&s_ncand, 1);
+      if (at < SEL_CAND) cand[at] = k; else s_over = 1;
+    }
   }
-  const int my_take = max(0, min(cnt[1], need - eq_before));
-  // ---- ordered compaction of my range ----
-  int eq_run = 0, sel_run = 0;
-  constexpr int IPT = 4;
+  cluster.sync();
+  int total_c = 0, over = 0;
+  for (int r = 0; r < CL; ++r) {
+    total_c += min(*cluster.map_shared_rank(&s_ncand, r), SEL_CAND + 1);
+    over |= *cluster.map_shared_rank(&s_over, r);
+  }
+  const bool fast = !over && total_c <= SEL_LEAD;
+  unsigned long long tau;
+  if (fast) {
+    if (crank == 0) {
+      int np = 1;
+      while (np < total_c) np <<= 1;
+      int base = 0;
+      for (int r = 0; r < CL; ++r) {
+        const int c = *cluster.map_shared_rank(&s_ncand, r);
+        const unsigned long long* pc = cluster.map_shared_rank(cand, r);
+        for (int i = tid; i < c; i += blockDim.x) lead[base + i] = pc[i];
+        base += c;
+      }
+      for (int i = total_c + tid; i < np; i += blockDim.x) lead[i] = 0ull;
+      __syncthreads();
+      bitonic_desc(lead, np);
+      if (tid == 0) s_tau = lead[need - 1];
+    }
+    cluster.sync();
+    tau = *cluster.map_shared_rank(&s_tau, 0);
+  } else {
+    // ---- slow path (crowded bucket): refine the key range level by level ----
+    unsigned long long base, width;
+    if (B0 < 64) { base = B0; width = 1; }
+    else {
+      int e = (B0 - 64) / 64 + 6, m = (B0 - 64) % 64;
+      base = (1ull << e) + ((unsigned long long)m << (e - 6));
+      width = 1ull << (e - 6);
+    }
+    while (width > 1) {
+      const int lw = 63 - __clzll((long long)width);
+      const int shift = lw > 12 ? lw - 12 : 0;
+      for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = 0;
+      __syncthreads();
+      for (int i = tid; i < cnt_local; i += blockDim.x) {
+        const unsigned long long k = key_at(i);
+        if (k >= base && k - base < width) hist_add(hist, (int)((k - base) >> shift));
+      }
+      cluster_find();
+      base += (unsigned long long)s_bin << shift;
+      need -= (int)s_above;
+      width = 1ull << shift;
+      cluster.sync();
+    }
+    tau = base;   // identical in every CTA of the cluster
+  }
+
+  // ---- emit: this CTA's selected tokens in ascending order, then place them ----
+  constexpr int IPT = 8;
+  int sel_run = 0;
   for (int t0 = 0; t0 < cnt_local; t0 += SEL_THREADS * IPT) {
-    int idx0 = t0 + threadIdx.x * IPT;
-    long long v[IPT];
-    int e_local = 0;
+    const int i0 = t0 + tid * IPT;
+    int flags = 0, c = 0;
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
-      int i = idx0 + k;
-      v[k] = (i < cnt_local) ? (cached ? cache[i] : s[lo + i]) : LLONG_MIN;
-      e_local += v[k] == tau;
+      const int i = i0 + k;
+      if (i < cnt_local && key_at(i) >= tau) { flags |= 1 << k; ++c; }
     }
-    int e_tot;
-    int e_before = block_excl_scan(e_local, warp_tot, &s_sum) + eq_run;
-    e_tot = s_sum;
-    int sflags = 0, s_local = 0;
-#pragma unroll
-    for (int k = 0; k < IPT; ++k) {
-      bool sel = v[k] > tau;
-      if (v[k] == tau) { sel = e_before < my_take; ++e_before; }
-      sflags |= (sel ? 1 : 0) << k;
-      s_local += sel;
-    }
-    int s_before = block_excl_scan(s_local, warp_tot, &s_sum) + sel_run;
-    int s_tot = s_sum;
+    int pos = block_excl_scan(c, warp_tot, &s_sum) + sel_run;
+    const int tile_tot = s_sum;
 #pragma unroll
     for (int k = 0; k < IPT; ++k)
-      if (sflags >> k & 1) {
-        const int pos = out_off + s_before++;
-        if (pos < K) out[pos] = lo + idx0 + k;
-        else set_status(D.status, HS_ERR_BAD_ID);
+      if (flags >> k & 1) {
+        if (pos < K) elist[pos] = lo + i0 + k;
+        ++pos;
       }
-    eq_run += e_tot;
-    sel_run += s_tot;
+    sel_run += tile_tot;
     __syncthreads();
   }
-  cluster.sync();   // peers may still read cnt[] until here
+  if (tid == 0) s_nsel = sel_run;
+  cluster.sync();
+  int off = 0;
+  for (int r = 0; r < crank; ++r) off += *cluster.map_shared_rank(&s_nsel, r);
+  for (int i = tid; i < sel_run; i += blockDim.x) {
+    if (off + i < K && i < K) out[off + i] = elist[i];
+    else set_status(D.status, HS_ERR_BAD_ID);
+  }
+  cluster.sync();   // peers may still read this CTA's shared memory until here
 }
 
 int num_sms() {
@@ -513,7 +615,8 @@ hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const 
       return HS_ERR_CUDA;
     attr = true;
   }
-  indexer_kernel<<<num_sms(), IX_THREADS, IX_SMEM, st>>>(p->d, il, n, d_req, d_limit, d_q, d_w, d_scores);
+  indexer_kernel<<<num_sms(), IX_THREADS, IX_SMEM, st>>>(p->d, il, n, d_req, d_limit, d_q, d_w, d_scores,
+                                                         p->cfg.max_ctx);
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -521,13 +624,27 @@ hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const 
                         int32_t* d_topk, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_SMEM) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return HS_ERR_CUDA;
     attr = true;
   }
-  select_kernel<<<n * SEL_CL, SEL_THREADS, SEL_SMEM, st>>>(p->d, scores, ld, d_limit, d_topk);
-  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  // 8 CTAs per token when their chunks fit the shared-memory cache, else 16
+  const int cl = (p->cfg.max_ctx <= 8 * SEL_CACHE) ? 8 : 16;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(n * cl, 1, 1);
+  lc.blockDim = dim3(SEL_THREADS, 1, 1);
+  lc.dynamicSmemBytes = SEL_SMEM;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, select_kernel, p->d, scores, ld, d_limit, d_topk) == cudaSuccess ? HS_OK
+                                                                                                  : HS_ERR_CUDA;
 }
 
 }  // namespace hs

@@ -53,8 +53,6 @@ struct Dev {
   int64_t* scores;      // [max_tokens, max_ctx]
   int4* miss_list;      // [max_tokens * topk] (layer-group row copies): {req, token, dst_row, 0}
   int32_t* miss_count;  // [max_tokens] misses recorded by the segment starting at each token
-  float* o_part;        // [max_tokens, MAX_SPLITS, n_heads, 512]
-  float2* ml_part;      // [max_tokens, MAX_SPLITS, n_heads] (max, sum) in log2 units
 };
 
 enum Counter { C_RESIDENT = 0, C_HITS = 1, C_MISSES = 2, C_H2D = 3, C_D2H = 4, C_N = 8 };

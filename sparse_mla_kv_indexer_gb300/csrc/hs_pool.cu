@@ -152,6 +152,7 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   if (c.num_pages < 1 || c.num_idx_pages < 1 || c.max_requests < 1 || c.max_ctx < 128 || c.max_ctx % 128)
     return HS_ERR_INVALID;
   if ((long long)c.num_pages * PAGE >= (1ll << 31)) return HS_ERR_INVALID;
+  if (c.max_ctx >= (1 << 21)) return HS_ERR_INVALID;   // token ids fit the 21-bit tie-break field
   if (c.max_q_per_req < 1 || c.max_q_per_req > 4 || c.max_q_per_req * c.topk > 8192) return HS_ERR_INVALID;
   if (c.max_q_per_req * c.n_idx_heads > 256) return HS_ERR_INVALID;
   if (c.hot_rows < PAGE || c.hot_rows % PAGE || c.hot_rows > 16384) return HS_ERR_INVALID;
@@ -208,8 +209,6 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   chk(dev_alloc(p, &D.scores, (size_t)c.max_tokens * c.max_ctx, 0));
   chk(dev_alloc(p, &D.miss_list, (size_t)c.max_tokens * c.topk, 0));
   chk(dev_alloc(p, &D.miss_count, (size_t)c.max_tokens, 0));
-  chk(dev_alloc(p, &D.o_part, (size_t)c.max_tokens * MAX_SPLITS * c.n_heads * 512, 0));
-  chk(dev_alloc(p, &D.ml_part, (size_t)c.max_tokens * MAX_SPLITS * c.n_heads, 0));
   if (s == HS_OK) {
     if (cudaMemcpy(D.kv, d_kv_layers, sizeof(void*) * c.n_layers, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(D.idx, d_idx_layers, sizeof(void*) * n_groups, cudaMemcpyHostToDevice) != cudaSuccess ||
