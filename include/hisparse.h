@@ -54,7 +54,8 @@ typedef enum hs_status {
   HS_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel gave up */
   HS_ERR_HOST_MISSING = 6, /* device: a placeholder page without a host copy was selected */
   HS_ERR_BAD_ID = 7,       /* device: a page, row or token id out of range */
-  HS_ERR_BAD_WEIGHT = 8    /* device: a negative index-head weight */
+  HS_ERR_BAD_WEIGHT = 8,   /* device: a negative index-head weight */
+  HS_ERR_SCRATCH_LIMIT = 9 /* request larger than the fixed scratch of hs_indexer_topk_noalloc */
 } hs_status;
 
 /* Pool geometry. Sizes are fixed for the pool's lifetime. */
@@ -198,6 +199,32 @@ hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, int32_t n_tokens,
  *  d_pool_pages [n] int32, d_host_pages [n] int64. */
 hs_status hs_offload_pages(hs_pool* pool, int32_t n, const int32_t* d_pool_pages,
                            const int64_t* d_host_pages, hs_stream_t stream);
+
+/* hs_indexer_topk for callers that cannot allocate device memory. The pages have
+ * no counterpart; this is a deployment variant of the call above.
+ * Who needs it: an engine that gives all free HBM to its KV pool before serving
+ * (a later cudaMalloc fails or fragments the pool), or code running while a
+ * stream is captured, where cudaMalloc is not allowed.
+ * What differs: the int64 score scratch is a fixed array inside the library,
+ * HS_NOALLOC_MAX_SCORES entries (16 MiB), held by every GPU that loads the
+ * library until the process exits; the call allocates nothing and uses no
+ * pool-owned scratch. Arguments and results are those of hs_indexer_topk
+ * without d_scores.
+ * Limits and rules:
+ *  - n_tokens * cfg.max_ctx must not exceed HS_NOALLOC_MAX_SCORES, otherwise the
+ *    call returns HS_ERR_SCRATCH_LIMIT and launches nothing;
+ *  - the pool's device must be current (HS_ERR_INVALID otherwise);
+ *  - the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture;
+ *  - every call on a device shares the one array, which keeps the previous
+ *    call's scores (each call writes every score it later reads, nothing needs
+ *    clearing); calls whose kernels overlap on the GPU, e.g. on two streams,
+ *    race on it and must be ordered by the caller. */
+#define HS_NOALLOC_MAX_SCORES (1ll << 21)
+hs_status hs_indexer_topk_noalloc(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
+                                  const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
+                                  const int8_t* d_w, int32_t* d_topk, hs_stream_t stream);
 
 /* Synchronise stream, return the first device-detected error since the last
  * call in *device_status and clear it. */

@@ -135,6 +135,7 @@ const char* hs_status_string(hs_status s) {
     case HS_ERR_HOST_MISSING: return "selected page has no host copy";
     case HS_ERR_BAD_ID: return "page, row or token id out of range";
     case HS_ERR_BAD_WEIGHT: return "negative index-head weight";
+    case HS_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation indexer";
   }
   return "unknown status";
 }

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhisparse
 STATUS = {
     0: "HS_OK", 1: "HS_ERR_INVALID", 2: "HS_ERR_OOM", 3: "HS_ERR_CAPACITY", 4: "HS_ERR_CUDA",
     5: "HS_ERR_TIMEOUT", 6: "HS_ERR_HOST_MISSING", 7: "HS_ERR_BAD_ID", 8: "HS_ERR_BAD_WEIGHT",
+    9: "HS_ERR_SCRATCH_LIMIT",
 }
 PLAN_PAD, PLAN_RESIDENT, PLAN_HIT, PLAN_MISS = 0, 1, 2, 3
 
@@ -53,6 +54,7 @@ _SIGS = {
     "hs_hot_release": [_P, _I, _P],
     "hs_append_rows": [_P, _I, _P, _P, _P, _P, _P],
     "hs_indexer_topk": [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P],
+    "hs_indexer_topk_noalloc": [_P, _I, _I, _P, _P, _P, _P, _P, _P],
     "hs_resolve_topk": [_P, _I, _I, _I, _P, _P, _P, _P, _P],
     "hs_sparse_mla_decode": [_P, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P],
     "hs_offload_pages": [_P, _I, _P, _P, _P],
@@ -154,6 +156,13 @@ class Pool:
     def indexer_topk(self, index_layer: int, req, limit, q, w, topk, scores=None, stream=None) -> None:
         _check("hs_indexer_topk", lib.hs_indexer_topk(self.handle, index_layer, req.numel(), _ptr(req), _ptr(limit),
                                                       _ptr(q), _ptr(w), _ptr(topk), _ptr(scores), _stream(stream)))
+
+    def indexer_topk_noalloc(self, index_layer: int, req, limit, q, w, topk, stream=None) -> None:
+        """hs_indexer_topk with its score scratch in the library's fixed array, for
+        callers that cannot allocate device memory (see include/hisparse.h)."""
+        _check("hs_indexer_topk_noalloc", lib.hs_indexer_topk_noalloc(
+            self.handle, index_layer, req.numel(), _ptr(req), _ptr(limit), _ptr(q), _ptr(w), _ptr(topk),
+            _stream(stream)))
 
     def resolve_topk(self, group: int, step: int, req, topk, row_ids, plan=None, stream=None) -> None:
         _check("hs_resolve_topk", lib.hs_resolve_topk(self.handle, group, step, req.numel(), _ptr(req), _ptr(topk),
