@@ -165,7 +165,8 @@ hs_status hs_append_rows(hs_pool* pool, int32_t n_tokens, const int32_t* d_req,
  *  d_q [n, H_i, 128] int8, d_w [n, H_i] int8 (must be >= 0).
  *  d_topk [n, K] int32 out: the K highest scores, ties to the lower token, in
  *  ascending token order; -1 pads when limit < K.
- *  d_scores nullable [n, max_ctx] int64 out: every score (entries >= limit undefined). */
+ *  d_scores nullable [n, max_ctx] int64 out, 16-byte aligned: every score (entries >= limit
+ *  undefined). */
 hs_status hs_indexer_topk(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
                           const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
                           const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,

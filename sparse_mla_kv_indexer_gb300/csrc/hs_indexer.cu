@@ -8,8 +8,9 @@
 // Scoring kernel (one persistent CTA per SM):
 //  * work item = (request segment, 128-key tile); the T <= 4 query tokens of a
 //    request share each key tile, so the keys are read from HBM once per request;
-//  * key pages (64 x 128 B) arrive by bulk copy (TMA unit) into a 4-stage ring
-//    filled by a producer warp; converter warps, an MMA warp and epilogue warps
+//  * key pages (64 x 128 B) arrive by bulk copy (TMA unit) into a ring of 6-12
+//    stages (all shared memory the query operand leaves free), filled by a
+//    producer warp that fetches page ids 32 tiles ahead; converter warps, an MMA warp and epilogue warps
 //    work on consecutive tiles at once (double-buffered A tiles and accumulators);
 //  * int8 keys and queries are widened to fp16 (exact for |x| <= 128) in the
 //    128-byte-swizzled K-major layout and contracted on the tensor cores with
@@ -38,23 +39,37 @@ namespace hs {
 // Warp roles (320 threads):
 //   warps 0-3  epilogue: TMEM accumulator -> ReLU, head weights, int64 scores
 //   warps 4-7  convert: raw int8 key tile -> fp16 A tile; queries -> fp16 B operand
-//   warp 8     producer: bulk copies of key pages into a 4-stage ring
+//   warp 8     producer: bulk copies of key pages into the stage ring
 //   warp 9     MMA issuer: tcgen05.mma into one of two TMEM accumulators
 constexpr int IX_THREADS = 320;
-constexpr int IX_STAGES = 4;
+constexpr int IX_MAX_STAGES = 12;
 constexpr int IX_TILE = 128;
 constexpr int IX_RAW = IX_TILE * IDX_DIM;              // 16 KB int8 per tile
 constexpr int IX_A_COL = IX_TILE * 128;                // one 64-dim fp16 atom column, 16 KB
 constexpr int IX_A = 2 * IX_A_COL;                     // 32 KB per A tile
-constexpr int IX_B_COL = 256 * 128;                    // B atom column for up to N = 256 rows
-constexpr int IX_MAX_SEG = 1024;
-constexpr int IX_OFF_A = 0;                            // 2 A tiles
-constexpr int IX_OFF_B = IX_OFF_A + 2 * IX_A;          // 64 KB
-constexpr int IX_OFF_RAW = IX_OFF_B + 2 * IX_B_COL;    // 128 KB
-constexpr int IX_OFF_BAR = IX_OFF_RAW + IX_STAGES * IX_RAW;   // 192 KB
-constexpr int IX_OFF_SEG = IX_OFF_BAR + 256;
-constexpr int IX_SMEM = IX_OFF_SEG + IX_MAX_SEG * 16 + 4 * 64 * 4 + 2 * IX_MAX_SEG * 4 + 1024;
+constexpr int IX_SMEM_BUDGET = 227 * 1024;
 constexpr int IX_TMEM_COLS = 512;                      // two accumulators of up to 256 columns
+
+// Shared-memory layout of one launch, sized by the batch geometry so the key
+// ring gets every byte the query operand does not need.
+struct IxLayout {
+  int b_col;      // bytes per 64-dim atom column of the query operand (n_max rows x 128 B)
+  int off_b, off_raw, off_bar, off_seg, stages, smem;
+};
+
+IxLayout ix_layout(int n_max_rows, int max_tokens) {
+  IxLayout L;
+  L.b_col = n_max_rows * 128;
+  L.off_b = 2 * IX_A;
+  L.off_raw = L.off_b + 2 * L.b_col;
+  const int tail = 512 + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  int stages = (IX_SMEM_BUDGET - L.off_raw - tail) / IX_RAW;
+  L.stages = stages > IX_MAX_STAGES ? IX_MAX_STAGES : stages;
+  L.off_bar = L.off_raw + L.stages * IX_RAW;
+  L.off_seg = L.off_bar + 512;
+  L.smem = L.off_seg + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  return L;
+}
 
 struct IxSeg {
   int32_t first;     // first token of the segment
@@ -91,25 +106,26 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __global__ void __launch_bounds__(IX_THREADS, 1)
 indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, const int32_t* __restrict__ limit_of,
                const int8_t* __restrict__ qg, const int8_t* __restrict__ wg, int64_t* __restrict__ scores,
-               int ld) {
+               int ld, IxLayout L) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + IX_OFF_BAR);
-  uint64_t* raw_full = bars;                      // [4]
-  uint64_t* raw_empty = bars + 4;                 // [4]
-  uint64_t* a_full = bars + 8;                    // [2]
-  uint64_t* a_empty = bars + 10;                  // [2]
-  uint64_t* t_full = bars + 12;                   // [2]
-  uint64_t* t_empty = bars + 14;                  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  const int NS = L.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  uint64_t* raw_full = bars;                      // [NS]
+  uint64_t* raw_empty = bars + IX_MAX_STAGES;     // [NS]
+  uint64_t* a_full = bars + 2 * IX_MAX_STAGES;    // [2]
+  uint64_t* a_empty = a_full + 2;                 // [2]
+  uint64_t* t_full = a_full + 4;                  // [2]
+  uint64_t* t_empty = a_full + 6;                 // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_full + 8);
   int32_t* s_nseg = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* s_dead = s_nseg + 1;
   int32_t* s_issued = s_nseg + 2;
   int32_t* s_consumed = s_nseg + 3;
-  IxSeg* segs = reinterpret_cast<IxSeg*>(smem + IX_OFF_SEG);
-  int32_t* s_w = reinterpret_cast<int32_t*>(smem + IX_OFF_SEG + IX_MAX_SEG * 16);   // [4][64], epilogue-owned
+  IxSeg* segs = reinterpret_cast<IxSeg*>(smem + L.off_seg);
+  int32_t* s_w = reinterpret_cast<int32_t*>(segs + D.max_tokens);                    // [4][64], epilogue-owned
   int32_t* s_req = s_w + 4 * 64;                                                      // [n_tok]
-  int32_t* s_lim = s_req + IX_MAX_SEG;                                                // [n_tok]
+  int32_t* s_lim = s_req + D.max_tokens;                                              // [n_tok]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hi = D.n_idx_heads;
@@ -145,7 +161,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
       segs[i].tile_end = tiles;
     }
     *s_nseg = ns;
-    for (int b = 0; b < 16; ++b) mbar_init(smem_u32(&bars[b]), 1);
+    for (int b = 0; b < 2 * IX_MAX_STAGES + 8; ++b) mbar_init(smem_u32(&bars[b]), 1);
     fence_mbar_init();
     *s_dead = 0;
     *s_issued = 0;
@@ -172,34 +188,53 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
 
   if (warp == 8) {
     // ------------------------------ producer ------------------------------
-    if (lane == 0) {
-      for (int i = 0; i < n_local; ++i) {
-        const int rs = i % IX_STAGES;
-        if (i >= IX_STAGES && !mbar_wait(smem_u32(&raw_empty[rs]), ((i / IX_STAGES) - 1) & 1, D.status)) {
-          *s_dead = 1;
-          break;
-        }
-        if (*(volatile int32_t*)s_dead) break;
+    // Lane l holds the key-page ids of tile (32c + l) of the current chunk c and
+    // of the next chunk, so no copy waits on a dependent page-table load.
+    auto fetch = [&](int i, int& p0, int& p1) {
+      p0 = p1 = -2;
+      if (i < n_local) {
         const int item = item_of(i);
         const int sg = seg_of(item);
         const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
-        const int r = s_req[segs[sg].first];
-        const uint32_t bar = smem_u32(&raw_full[rs]);
-        const uint32_t dst = smem_u32(smem + IX_OFF_RAW + rs * IX_RAW);
-        const int npg = ((tile * IX_TILE + PAGE) < segs[sg].maxlim) ? 2 : 1;
-        int ip[2] = {-1, -1};
-        uint32_t bytes = 0;
-        for (int k = 0; k < npg; ++k) {
-          int v = D.idx_bt[(size_t)r * D.max_pages + tile * 2 + k];
-          if (v < 0 || v >= D.num_idx_pages) { set_status(D.status, HS_ERR_BAD_ID); continue; }
-          ip[k] = v;
-          bytes += IDX_PAGE_BYTES;
-        }
-        mbar_expect_tx(bar, bytes);
-        for (int k = 0; k < 2; ++k)
-          if (ip[k] >= 0) bulk_g2s(dst + k * IDX_PAGE_BYTES, keys + (size_t)ip[k] * IDX_PAGE_BYTES, IDX_PAGE_BYTES, bar);
-        *s_issued = i + 1;
+        const int32_t* bt = D.idx_bt + (size_t)s_req[segs[sg].first] * D.max_pages + tile * 2;
+        p0 = bt[0];
+        p1 = ((tile * IX_TILE + PAGE) < segs[sg].maxlim) ? bt[1] : -2;   // -2: page beyond the limit
       }
+    };
+    int c0, c1, n0, n1;
+    fetch(lane, c0, c1);
+    fetch(32 + lane, n0, n1);
+    for (int i = 0; i < n_local; ++i) {
+      if (i > 0 && (i & 31) == 0) {
+        c0 = n0;
+        c1 = n1;
+        fetch(i + 32 + lane, n0, n1);
+      }
+      const int ip0 = __shfl_sync(0xffffffffu, c0, i & 31);
+      const int ip1 = __shfl_sync(0xffffffffu, c1, i & 31);
+      int dead = 0;
+      if (lane == 0) {
+        const int rs = i % NS;
+        if (i >= NS && !mbar_wait(smem_u32(&raw_empty[rs]), ((i / NS) - 1) & 1, D.status)) *s_dead = 1;
+        dead = *(volatile int32_t*)s_dead;
+        if (!dead) {
+          const uint32_t bar = smem_u32(&raw_full[rs]);
+          const uint32_t dst = smem_u32(smem + L.off_raw + rs * IX_RAW);
+          const int ips[2] = {ip0, ip1};
+          uint32_t bytes = 0;
+          for (int k = 0; k < 2; ++k) {
+            if (ips[k] == -2) continue;
+            if (ips[k] < 0 || ips[k] >= D.num_idx_pages) { set_status(D.status, HS_ERR_BAD_ID); continue; }
+            bytes += IDX_PAGE_BYTES;
+          }
+          mbar_expect_tx(bar, bytes);
+          for (int k = 0; k < 2; ++k)
+            if (ips[k] >= 0 && ips[k] < D.num_idx_pages)
+              bulk_g2s(dst + k * IDX_PAGE_BYTES, keys + (size_t)ips[k] * IDX_PAGE_BYTES, IDX_PAGE_BYTES, bar);
+          *s_issued = i + 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, dead, 0)) break;
     }
   } else if (warp == 9) {
     // ------------------------------ MMA issuer ------------------------------
@@ -213,11 +248,11 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
         const IxSeg S = segs[seg_of(item_of(i))];
         const int N = ((S.ntok * Hi) + 15) & ~15;
         const uint32_t idesc = idesc_f16(128, N, false, false);
-        const uint32_t a0 = smem_u32(smem + IX_OFF_A + ab * IX_A), b0 = smem_u32(smem + IX_OFF_B);
+        const uint32_t a0 = smem_u32(smem + ab * IX_A), b0 = smem_u32(smem + L.off_b);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * IX_A_COL + (kk & 3) * 32, 16, 1024);
-          uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * IX_B_COL + (kk & 3) * 32, 16, 1024);
+          uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * L.b_col + (kk & 3) * 32, 16, 1024);
           umma_f16(tmem + ab * 256, ad, bd, idesc, kk > 0);
         }
         umma_commit(smem_u32(&a_empty[ab]));
@@ -238,7 +273,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
       if (sg != cur_seg) {
         // every MMA reading the previous queries has completed before they are replaced
         if (i > 0) ok = mbar_wait(smem_u32(&a_empty[(i - 1) & 1]), ((i - 1) >> 1) & 1, D.status);
-        uint8_t* B = smem + IX_OFF_B;
+        uint8_t* B = smem + L.off_b;
         const int N = ((S.ntok * Hi) + 15) & ~15;
         for (int c = ct; c < N * 8; c += 128) {
           const int row = c >> 3, ch16 = c & 7;       // 8 chunks of 16 int8 per 128-dim row
@@ -250,19 +285,19 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
           uint4 c0, c1;
           i8x16_to_f16(v, c0, c1);
           const int dim0 = ch16 * 16;
-          uint8_t* base = B + (dim0 >> 6) * IX_B_COL;
+          uint8_t* base = B + (dim0 >> 6) * L.b_col;
           const int chunk = (dim0 & 63) >> 3;
           *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk)) = c0;
           *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk + 1)) = c1;
         }
         cur_seg = sg;
       }
-      const int rs = i % IX_STAGES, ab = i & 1;
-      if (ok) ok = mbar_wait(smem_u32(&raw_full[rs]), (i / IX_STAGES) & 1, D.status);
+      const int rs = i % NS, ab = i & 1;
+      if (ok) ok = mbar_wait(smem_u32(&raw_full[rs]), (i / NS) & 1, D.status);
       if (ok && i >= 2) ok = mbar_wait(smem_u32(&a_empty[ab]), ((i >> 1) - 1) & 1, D.status);
       if (!ok) *s_dead = 1;
-      const uint8_t* raw = smem + IX_OFF_RAW + rs * IX_RAW;
-      uint8_t* A = smem + IX_OFF_A + ab * IX_A;
+      const uint8_t* raw = smem + L.off_raw + rs * IX_RAW;
+      uint8_t* A = smem + ab * IX_A;
       for (int c = ct; c < IX_TILE * 8; c += 128) {
         const int row = c >> 3, ch16 = c & 7;
         uint4 v = make_uint4(0, 0, 0, 0);
@@ -336,7 +371,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   if (*s_dead && tid == 8 * 32) {
     // drain bulk copies still in flight before the CTA's shared memory goes away
     for (int k = *s_consumed; k < *s_issued; ++k)
-      mbar_wait(smem_u32(&raw_full[k % IX_STAGES]), (k / IX_STAGES) & 1, D.status);
+      mbar_wait(smem_u32(&raw_full[k % NS]), (k / NS) & 1, D.status);
   }
   tc_fence_before();
   __syncthreads();
@@ -353,10 +388,10 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
 // K-th largest key tau selects them with the single test key >= tau.
 constexpr int SEL_THREADS = 512;
 constexpr int SEL_BINS = 4096;
-constexpr int SEL_CACHE = 20480;                       // keys cached in shared memory per CTA
+constexpr int SEL_CACHE = 12288;                       // keys cached in shared memory per CTA
 constexpr int SEL_CAND = 2048;                         // candidates per CTA on the fast path
 constexpr int SEL_LEAD = 4096;                         // candidates the cluster leader sorts
-constexpr int SEL_SMEM = SEL_CACHE * 8 + SEL_LEAD * 8 + 1024;
+constexpr int SEL_SMEM = SEL_CACHE * 8 + SEL_CACHE * 2 + SEL_LEAD * 8 + SEL_CAND * 8 + 1024;
 constexpr unsigned long long IDX_MASK = (1ull << 21) - 1;
 
 // monotone level-0 bucket of a key: exact below 64, then 64 buckets per octave
@@ -367,12 +402,9 @@ __device__ __forceinline__ int bucket1(unsigned long long v) {
   return 64 + (e - 6) * 64 + m;
 }
 
-// warp-aggregated shared-memory histogram increment
-__device__ __forceinline__ void hist_add(uint32_t* hist, int bin) {
-  const unsigned act = __activemask();
-  const unsigned peers = __match_any_sync(act, bin);
-  if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-}
+// shared-memory histogram increment (scores spread over many buckets, so plain
+// atomics rarely collide within a warp)
+__device__ __forceinline__ void hist_add(uint32_t* hist, int bin) { atomicAdd(&hist[bin], 1u); }
 
 __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -416,26 +448,30 @@ __device__ void bitonic_desc(unsigned long long* a, int n) {
     }
 }
 
+template <int CL>
 __global__ void __launch_bounds__(SEL_THREADS, 1)
 select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of,
               int32_t* __restrict__ topk) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int crank = (int)cluster.block_rank();
-  const int CL = (int)cluster.num_blocks();
-  const int slice = SEL_BINS / CL;
+  uint32_t crank_u;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank_u));
+  const int crank = (int)crank_u;
+  constexpr int slice = SEL_BINS / CL;
   const int tok = blockIdx.x / CL;
   const int K = D.topk;
   const int tid = threadIdx.x;
-  __shared__ uint32_t hist[SEL_BINS];      // level histograms; later the candidate list
-  __shared__ uint32_t tot[SEL_BINS / 8];
+  __shared__ uint32_t hist[SEL_BINS];      // level histograms (own partial, then cluster totals)
+  __shared__ uint32_t tot[slice];          // cluster totals of this CTA's slice of bins
   __shared__ int warp_tot[32];
-  __shared__ int s_sum, s_bin, s_ncand, s_over, s_nsel;
+  __shared__ int s_sum, s_bin, s_ncand, s_over, s_nsel, s_off, s_total_c, s_any_over;
+  __shared__ int s_cnt[CL];
   __shared__ long long s_above;
   __shared__ unsigned long long s_tau;
+  __shared__ __align__(8) uint64_t s_bar;
   extern __shared__ __align__(16) uint8_t sel_dyn[];
   unsigned long long* cache = reinterpret_cast<unsigned long long*>(sel_dyn);            // [SEL_CACHE]
   unsigned long long* lead = cache + SEL_CACHE;                                           // [SEL_LEAD]
-  unsigned long long* cand = reinterpret_cast<unsigned long long*>(hist);                 // [SEL_CAND]
+  unsigned long long* cand = lead + SEL_LEAD;                                             // [SEL_CAND]
+  uint16_t* bk = reinterpret_cast<uint16_t*>(cand + SEL_CAND);                            // [SEL_CACHE] buckets
   int32_t* elist = reinterpret_cast<int32_t*>(lead);                                      // [K] after tau
 
   int n = limit_of[tok];
@@ -447,8 +483,8 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
     return;
   }
   const long long* s = reinterpret_cast<const long long*>(scores) + (size_t)tok * ld;
-  const int per = (n + CL - 1) / CL;
-  const int lo = crank * per, hi = min(n, lo + per);
+  const int per = ((n + CL - 1) / CL + 1) & ~1;   // even, so every chunk starts 16-byte aligned
+  const int lo = min(n, crank * per), hi = min(n, lo + per);
   const int cnt_local = max(0, hi - lo);
   const bool cached = per <= SEL_CACHE;
   auto key_at = [&](int i) -> unsigned long long {
@@ -459,35 +495,74 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
 
   // ---- level 0: histogram of bucket1(key); find the bucket of the K-th largest ----
   for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = 0;
-  if (tid == 0) { s_ncand = 0; s_over = 0; s_bin = 0; s_above = 0; }
+  if (tid == 0) {
+    s_ncand = 0; s_over = 0; s_bin = 0; s_above = 0;
+    if (cached) {
+      mbar_init(smem_u32(&s_bar), 1);
+      fence_mbar_init();
+    }
+  }
   __syncthreads();
-  for (int i = tid; i < cnt_local; i += blockDim.x) {
-    long long v = s[lo + i];
-    if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
-    const unsigned long long k = ((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + i));
-    if (cached) cache[i] = k;
-    hist_add(hist, bucket1(k));
+  if (cached) {
+    // the whole chunk arrives by bulk copy (TMA unit) in one round trip
+    const int even = cnt_local & ~1;
+    if (tid == 0) {
+      const uint32_t bar = smem_u32(&s_bar);
+      mbar_expect_tx(bar, (uint32_t)even * 8u);
+      for (int off = 0; off < even; off += 4096)
+        bulk_g2s(smem_u32(cache + off), s + lo + off, (uint32_t)min(4096, even - off) * 8u, bar);
+    }
+    if (tid == 0 && (cnt_local & 1)) cache[cnt_local - 1] = (unsigned long long)s[lo + cnt_local - 1];
+    if (!mbar_wait(smem_u32(&s_bar), 0, D.status)) { /* recorded; the data below is then unreliable */ }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = tid; i < cnt_local; i += blockDim.x) {
+      long long v = (long long)cache[i];
+      if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
+      const unsigned long long k = ((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + i));
+      cache[i] = k;
+      const int b = bucket1(k);
+      bk[i] = (uint16_t)b;
+      hist_add(hist, b);
+    }
+  } else {
+    for (int i = tid; i < cnt_local; i += blockDim.x) {
+      long long v = s[lo + i];
+      if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
+      hist_add(hist, bucket1(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + i))));
+    }
   }
   int need = K;
   auto cluster_find = [&](void) {
-    cluster.sync();
+    cluster_sync();
     for (int b = tid; b < slice; b += blockDim.x) {
+      uint32_t part[CL];
+#pragma unroll
+      for (int r = 0; r < CL; ++r) part[r] = ld_cluster_u32(mapa(smem_u32(hist + crank * slice + b), r));
       uint32_t a = 0;
-      for (int r = 0; r < CL; ++r) a += cluster.map_shared_rank(hist, r)[crank * slice + b];
+#pragma unroll
+      for (int r = 0; r < CL; ++r) a += part[r];
       tot[b] = a;
     }
-    cluster.sync();
-    for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = cluster.map_shared_rank(tot, b / slice)[b % slice];
+    cluster_sync();
+    constexpr int PER = SEL_BINS / SEL_THREADS;   // 8 bins per thread
+    uint32_t t[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int b = tid + k * SEL_THREADS;
+      t[k] = ld_cluster_u32(mapa(smem_u32(tot + b % slice), b / slice));
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) hist[tid + k * SEL_THREADS] = t[k];
     if (tid == 0) { s_bin = 0; s_above = 0; }
     __syncthreads();
-    const int per_t = SEL_BINS / SEL_THREADS;     // 8 bins per thread, thread 0 = top bins
     int local = 0;
-    for (int k = 0; k < per_t; ++k) local += hist[SEL_BINS - 1 - (tid * per_t + k)];
+    for (int k = 0; k < PER; ++k) local += hist[SEL_BINS - 1 - (tid * PER + k)];
     int before = block_excl_scan(local, warp_tot, nullptr);
     if (before < need && need <= before + local) {
       int cum = before;
-      for (int k = 0; k < per_t; ++k) {
-        int b = SEL_BINS - 1 - (tid * per_t + k);
+      for (int k = 0; k < PER; ++k) {
+        int b = SEL_BINS - 1 - (tid * PER + k);
         if (cum + (int)hist[b] >= need) { s_bin = b; s_above = cum; break; }
         cum += hist[b];
       }
@@ -497,44 +572,51 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   cluster_find();
   const int B0 = s_bin;
   need -= (int)s_above;
-  cluster.sync();           // every CTA is done reading peers' tot[] / hist[] of level 0
 
   // ---- fast path: collect the keys of bucket B0, the leader sorts them ----
-  if (tid == 0) s_ncand = 0;
-  __syncthreads();
+#pragma unroll 4
   for (int i = tid; i < cnt_local; i += blockDim.x) {
-    const unsigned long long k = key_at(i);
-    if (bucket1(k) == B0) {
+    if (cached ? bk[i] == B0 : bucket1(key_at(i)) == B0) {
+      const unsigned long long k = key_at(i);
       int at = atomicAdd(&s_ncand, 1);
       if (at < SEL_CAND) cand[at] = k; else s_over = 1;
     }
   }
-  cluster.sync();
-  int total_c = 0, over = 0;
-  for (int r = 0; r < CL; ++r) {
-    total_c += min(*cluster.map_shared_rank(&s_ncand, r), SEL_CAND + 1);
-    over |= *cluster.map_shared_rank(&s_over, r);
+  cluster_sync();
+  if (tid < 32) {
+    int c = 0, o = 0;
+    if (tid < CL) {
+      c = (int)ld_cluster_u32(mapa(smem_u32(&s_ncand), tid));
+      o = (int)ld_cluster_u32(mapa(smem_u32(&s_over), tid));
+      s_cnt[tid] = c;
+    }
+    const int tc = __reduce_add_sync(0xffffffffu, min(c, SEL_CAND + 1));
+    const int to = __reduce_or_sync(0xffffffffu, o);
+    if (tid == 0) { s_total_c = tc; s_any_over = to; }
   }
-  const bool fast = !over && total_c <= SEL_LEAD;
+  __syncthreads();
+  const int total_c = s_total_c;
+  const bool fast = !s_any_over && total_c <= SEL_LEAD;
   unsigned long long tau;
   if (fast) {
     if (crank == 0) {
       int np = 1;
       while (np < total_c) np <<= 1;
-      int base = 0;
-      for (int r = 0; r < CL; ++r) {
-        const int c = *cluster.map_shared_rank(&s_ncand, r);
-        const unsigned long long* pc = cluster.map_shared_rank(cand, r);
-        for (int i = tid; i < c; i += blockDim.x) lead[base + i] = pc[i];
-        base += c;
+      // warp r copies peer r's candidates
+      const int warp = tid >> 5, lane = tid & 31;
+      if (warp < CL) {
+        int base = 0;
+        for (int r = 0; r < warp; ++r) base += s_cnt[r];
+        const uint32_t pc = mapa(smem_u32(cand), warp);
+        for (int i = lane; i < s_cnt[warp]; i += 32) lead[base + i] = ld_cluster_u64(pc + 8u * i);
       }
       for (int i = total_c + tid; i < np; i += blockDim.x) lead[i] = 0ull;
       __syncthreads();
       bitonic_desc(lead, np);
       if (tid == 0) s_tau = lead[need - 1];
     }
-    cluster.sync();
-    tau = *cluster.map_shared_rank(&s_tau, 0);
+    cluster_sync();
+    tau = ld_cluster_u64(mapa(smem_u32(&s_tau), 0));
   } else {
     // ---- slow path (crowded bucket): refine the key range level by level ----
     unsigned long long base, width;
@@ -547,6 +629,7 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
     while (width > 1) {
       const int lw = 63 - __clzll((long long)width);
       const int shift = lw > 12 ? lw - 12 : 0;
+      cluster_sync();     // peers finished reading tot[] of the previous level
       for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = 0;
       __syncthreads();
       for (int i = tid; i < cnt_local; i += blockDim.x) {
@@ -557,42 +640,52 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
       base += (unsigned long long)s_bin << shift;
       need -= (int)s_above;
       width = 1ull << shift;
-      cluster.sync();
     }
     tau = base;   // identical in every CTA of the cluster
   }
 
   // ---- emit: this CTA's selected tokens in ascending order, then place them ----
-  constexpr int IPT = 8;
+  // warp w owns a contiguous range of the chunk; one prefix over warp counts
+  // orders the warps, ballots order the lanes.
+  const int lane = tid & 31, wid = tid >> 5;
+  constexpr int NW = SEL_THREADS / 32;
+  const int wper = (cnt_local + NW - 1) / NW;
+  const int wlo = min(cnt_local, wid * wper), whi = min(cnt_local, wlo + wper);
+  int wcount = 0;
+#pragma unroll 4
+  for (int i = wlo + lane; i < whi; i += 32) wcount += key_at(i) >= tau;
+  wcount = __reduce_add_sync(0xffffffffu, wcount);
+  if (lane == 0) warp_tot[wid] = wcount;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < wid; ++w) wbase += warp_tot[w];
   int sel_run = 0;
-  for (int t0 = 0; t0 < cnt_local; t0 += SEL_THREADS * IPT) {
-    const int i0 = t0 + tid * IPT;
-    int flags = 0, c = 0;
-#pragma unroll
-    for (int k = 0; k < IPT; ++k) {
-      const int i = i0 + k;
-      if (i < cnt_local && key_at(i) >= tau) { flags |= 1 << k; ++c; }
+  for (int w = 0; w < NW; ++w) sel_run += warp_tot[w];
+  for (int i0 = wlo; i0 < whi; i0 += 32) {
+    const int i = i0 + lane;
+    const bool sel = i < whi && key_at(i) >= tau;
+    const unsigned m = __ballot_sync(0xffffffffu, sel);
+    if (sel) {
+      const int pos = wbase + __popc(m & ((1u << lane) - 1));
+      if (pos < K) elist[pos] = lo + i;
     }
-    int pos = block_excl_scan(c, warp_tot, &s_sum) + sel_run;
-    const int tile_tot = s_sum;
-#pragma unroll
-    for (int k = 0; k < IPT; ++k)
-      if (flags >> k & 1) {
-        if (pos < K) elist[pos] = lo + i0 + k;
-        ++pos;
-      }
-    sel_run += tile_tot;
-    __syncthreads();
+    wbase += __popc(m);
   }
+  __syncthreads();
   if (tid == 0) s_nsel = sel_run;
-  cluster.sync();
-  int off = 0;
-  for (int r = 0; r < crank; ++r) off += *cluster.map_shared_rank(&s_nsel, r);
+  cluster_sync();
+  if (tid < 32) {
+    const int c = (tid < crank) ? (int)ld_cluster_u32(mapa(smem_u32(&s_nsel), tid)) : 0;
+    const int off = __reduce_add_sync(0xffffffffu, c);
+    if (tid == 0) s_off = off;
+  }
+  __syncthreads();
+  const int off = s_off;
   for (int i = tid; i < sel_run; i += blockDim.x) {
     if (off + i < K && i < K) out[off + i] = elist[i];
     else set_status(D.status, HS_ERR_BAD_ID);
   }
-  cluster.sync();   // peers may still read this CTA's shared memory until here
+  cluster_sync();   // peers may still read this CTA's shared memory until here
 }
 
 int num_sms() {
@@ -608,43 +701,52 @@ int num_sms() {
 
 hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
                          const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, IX_SMEM) !=
-        cudaSuccess)
+  const int n_max = ((p->cfg.max_q_per_req * p->cfg.n_idx_heads) + 15) & ~15;
+  const IxLayout L = ix_layout(n_max, p->cfg.max_tokens);
+  if (L.stages < 2) return HS_ERR_INVALID;
+  static int attr_smem = 0;
+  if (attr_smem < L.smem) {
+    if (cudaFuncSetAttribute(indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem) != cudaSuccess)
       return HS_ERR_CUDA;
-    attr = true;
+    attr_smem = L.smem;
   }
-  indexer_kernel<<<num_sms(), IX_THREADS, IX_SMEM, st>>>(p->d, il, n, d_req, d_limit, d_q, d_w, d_scores,
-                                                         p->cfg.max_ctx);
+  indexer_kernel<<<num_sms(), IX_THREADS, L.smem, st>>>(p->d, il, n, d_req, d_limit, d_q, d_w, d_scores,
+                                                        p->cfg.max_ctx, L);
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
-hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                        int32_t* d_topk, cudaStream_t st) {
+template <int CL>
+hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                           int32_t* d_topk, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    if (cudaFuncSetAttribute(select_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(select_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return HS_ERR_CUDA;
     attr = true;
   }
-  // 8 CTAs per token when their chunks fit the shared-memory cache, else 16
-  const int cl = (p->cfg.max_ctx <= 8 * SEL_CACHE) ? 8 : 16;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(n * cl, 1, 1);
+  lc.gridDim = dim3(n * CL, 1, 1);
   lc.blockDim = dim3(SEL_THREADS, 1, 1);
   lc.dynamicSmemBytes = SEL_SMEM;
   lc.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = cl;
+  at[0].val.clusterDim.x = CL;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, select_kernel, p->d, scores, ld, d_limit, d_topk) == cudaSuccess ? HS_OK
-                                                                                                  : HS_ERR_CUDA;
+  return cudaLaunchKernelEx(&lc, select_kernel<CL>, p->d, scores, ld, d_limit, d_topk) == cudaSuccess
+             ? HS_OK
+             : HS_ERR_CUDA;
+}
+
+hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                        int32_t* d_topk, cudaStream_t st) {
+  // 16 CTAs per token: each CTA's chunk is smaller and every pass shorter
+  return launch_select_cl<16>(p, n, scores, ld, d_limit, d_topk, st);
 }
 
 }  // namespace hs

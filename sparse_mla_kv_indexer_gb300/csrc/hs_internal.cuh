@@ -53,6 +53,7 @@ struct Dev {
   int64_t* scores;      // [max_tokens, max_ctx]
   int4* miss_list;      // [max_tokens * topk] (layer-group row copies): {req, token, dst_row, 0}
   int32_t* miss_count;  // [max_tokens] misses recorded by the segment starting at each token
+  __half* o_part;       // [max_tokens, MAX_SPLITS, 512, 64] fp16 partial attention outputs
 };
 
 enum Counter { C_RESIDENT = 0, C_HITS = 1, C_MISSES = 2, C_H2D = 3, C_D2H = 4, C_N = 8 };
@@ -203,12 +204,47 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
   d |= (uint64_t)2 << 61;          // 128-byte swizzle
   return d;
 }
-// Instruction descriptor, kind::f16 with fp16 A and B and fp32 accumulation.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor, kind::f16 with fp16 (or bf16) A and B and fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                 bool bf16 = false) {
   return (1u << 4)                                   // D = f32
-         | (0u << 7) | (0u << 10)                    // A, B = f16
+         | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10)   // A, B = f16 or bf16
          | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16)
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---- distributed shared memory (thread-block clusters) ---------------------------
+// Cluster-wide barrier with release/acquire ordering of shared-memory accesses.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+// 16-byte global load that bypasses the non-coherent path (data written by this kernel).
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // Byte offset of 16-bit element (row, col) inside a [rows x 64] SW128 block

@@ -210,6 +210,7 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   chk(dev_alloc(p, &D.scores, (size_t)c.max_tokens * c.max_ctx, 0));
   chk(dev_alloc(p, &D.miss_list, (size_t)c.max_tokens * c.topk, 0));
   chk(dev_alloc(p, &D.miss_count, (size_t)c.max_tokens, 0));
+  chk(dev_alloc(p, &D.o_part, (size_t)c.max_tokens * MAX_SPLITS * 512 * 64, 0));
   if (s == HS_OK) {
     if (cudaMemcpy(D.kv, d_kv_layers, sizeof(void*) * c.n_layers, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(D.idx, d_idx_layers, sizeof(void*) * n_groups, cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -302,6 +303,7 @@ hs_status hs_indexer_topk(hs_pool* p, int32_t index_layer, int32_t n, const int3
   if (!p || index_layer < 0 || index_layer >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   if (n == 0) return HS_OK;
   if (!d_req || !d_limit || !d_q || !d_w || !d_topk || !aligned16(d_q)) return HS_ERR_INVALID;
+  if (d_scores && !aligned16(d_scores)) return HS_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int64_t* scores = d_scores ? d_scores : p->d.scores;
   hs_status s = launch_indexer(p, index_layer, n, d_req, d_limit, d_q, d_w, scores, st);
