@@ -125,6 +125,8 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     fence_mbar_init();
     *s_flag = 0;
   }
+  griddep_wait();
+  griddep_launch();
   if (tid < ATTN_ROWS) {
     const int k = (int)split * ATTN_ROWS + tid;
     int id = k < K ? row_ids[(size_t)tok * K + k] : -1;
@@ -376,22 +378,8 @@ hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, co
     attr = true;
   }
   const int n_splits = (p->cfg.topk + ATTN_ROWS - 1) / ATTN_ROWS;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(n_splits, n, 1);
-  lc.blockDim = dim3(AT_THREADS, 1, 1);
-  lc.dynamicSmemBytes = AT_SMEM;
-  lc.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = n_splits;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  if (cudaLaunchKernelEx(&lc, attention_kernel, p->d, layer, d_q, d_rows, sm_scale * LOG2E, d_out, d_lse) !=
-      cudaSuccess)
-    return HS_ERR_CUDA;
-  return HS_OK;
+  return launch_pdl(attention_kernel, dim3(n_splits, n, 1), dim3(AT_THREADS, 1, 1), AT_SMEM, st, n_splits, p->d, layer,
+                    d_q, d_rows, sm_scale * LOG2E, d_out, d_lse);
 }
 
 }  // namespace hs

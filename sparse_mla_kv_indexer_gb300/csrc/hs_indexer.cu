@@ -131,6 +131,13 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   const int Hi = D.n_idx_heads;
   const int8_t* keys = D.idx[il];
 
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), IX_TMEM_COLS);
+  if (tid == 0) {
+    for (int b = 0; b < 2 * IX_MAX_STAGES + 8; ++b) mbar_init(smem_u32(&bars[b]), 1);
+    fence_mbar_init();
+  }
+  griddep_wait();
+  griddep_launch();
   // ---- request segments of the batch (tokens of one request are contiguous) ----
   for (int t = tid; t < n_tok; t += IX_THREADS) {
     int r = req_of[t], lim = limit_of[t];
@@ -161,13 +168,10 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
       segs[i].tile_end = tiles;
     }
     *s_nseg = ns;
-    for (int b = 0; b < 2 * IX_MAX_STAGES + 8; ++b) mbar_init(smem_u32(&bars[b]), 1);
-    fence_mbar_init();
     *s_dead = 0;
     *s_issued = 0;
     *s_consumed = 0;
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), IX_TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -474,6 +478,8 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   uint16_t* bk = reinterpret_cast<uint16_t*>(cand + SEL_CAND);                            // [SEL_CACHE] buckets
   int32_t* elist = reinterpret_cast<int32_t*>(lead);                                      // [K] after tau
 
+  griddep_wait();
+  griddep_launch();
   int n = limit_of[tok];
   n = max(0, min(n, D.max_ctx));
   int32_t* out = topk + (size_t)tok * K;
@@ -710,9 +716,8 @@ hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const 
       return HS_ERR_CUDA;
     attr_smem = L.smem;
   }
-  indexer_kernel<<<num_sms(), IX_THREADS, L.smem, st>>>(p->d, il, n, d_req, d_limit, d_q, d_w, d_scores,
-                                                        p->cfg.max_ctx, L);
-  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  return launch_pdl(indexer_kernel, dim3(num_sms()), dim3(IX_THREADS), L.smem, st, 0, p->d, il, n, d_req, d_limit,
+                    d_q, d_w, d_scores, p->cfg.max_ctx, L);
 }
 
 template <int CL>
@@ -726,21 +731,8 @@ hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, con
       return HS_ERR_CUDA;
     attr = true;
   }
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(n * CL, 1, 1);
-  lc.blockDim = dim3(SEL_THREADS, 1, 1);
-  lc.dynamicSmemBytes = SEL_SMEM;
-  lc.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, select_kernel<CL>, p->d, scores, ld, d_limit, d_topk) == cudaSuccess
-             ? HS_OK
-             : HS_ERR_CUDA;
+  return launch_pdl(select_kernel<CL>, dim3(n * CL), dim3(SEL_THREADS), SEL_SMEM, st, CL, p->d, scores, ld, d_limit,
+                    d_topk);
 }
 
 hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,

@@ -257,6 +257,39 @@ __host__ __device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
   return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
 }
 
+// ---- programmatic dependent launch -------------------------------------------------
+// A hot-path kernel may start while its predecessor in the stream finishes; it
+// runs its address-independent prologue, then waits for the predecessor's
+// completion (and memory) before touching global data, then lets its own
+// successor start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            int cluster_x, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster_x > 0) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = cluster_x;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  lc.attrs = at;
+  lc.numAttrs = na;
+  return cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
 // ---- host-side launch helpers (defined in hs_pool.cu) ----------------------------
 hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
                          const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, cudaStream_t st);

@@ -43,6 +43,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // ---- append: new KV rows (all layers) and index keys (all indexer layers) ----
 __global__ void append_kernel(Dev D, int n, const int32_t* __restrict__ req_of, const int32_t* __restrict__ pos_of,
                               const uint8_t* __restrict__ kv_rows, const int8_t* __restrict__ idx_keys) {
+  griddep_wait();
+  griddep_launch();
   const long long kv_chunks = (long long)n * D.n_layers * ROW_CHUNKS;
   const long long ix_chunks = (long long)n * D.n_groups * (IDX_DIM / 16);
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < kv_chunks + ix_chunks;
@@ -77,6 +79,8 @@ __global__ void append_kernel(Dev D, int n, const int32_t* __restrict__ req_of, 
 // ---- page materialisation: pool page -> host page, every sparse layer ----
 __global__ void offload_kernel(Dev D, int n, const int32_t* __restrict__ pool_pages,
                                const int64_t* __restrict__ host_pages) {
+  griddep_wait();
+  griddep_launch();
   constexpr int PAGE_CHUNKS = PAGE * ROW / 16;   // 2,624 per page per layer
   const long long total = (long long)n * D.n_layers * PAGE_CHUNKS;
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < total;
@@ -292,9 +296,8 @@ hs_status hs_append_rows(hs_pool* p, int32_t n, const int32_t* d_req, const int3
   if (!d_req || !d_pos || !d_kv_rows || !d_idx_keys || !aligned16(d_kv_rows) || !aligned16(d_idx_keys))
     return HS_ERR_INVALID;
   const long long work = (long long)n * (p->d.n_layers * ROW_CHUNKS + p->d.n_groups * (IDX_DIM / 16));
-  append_kernel<<<launch_blocks(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p->d, n, d_req, d_pos,
-                                                                                            d_kv_rows, d_idx_keys);
-  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  return launch_pdl(append_kernel, dim3(launch_blocks(work, 256)), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                    0, p->d, n, d_req, d_pos, d_kv_rows, d_idx_keys);
 }
 
 hs_status hs_indexer_topk(hs_pool* p, int32_t index_layer, int32_t n, const int32_t* d_req, const int32_t* d_limit,
@@ -333,9 +336,8 @@ hs_status hs_offload_pages(hs_pool* p, int32_t n, const int32_t* d_pool_pages, c
   if (n == 0) return HS_OK;
   if (!d_pool_pages || !d_host_pages) return HS_ERR_INVALID;
   const long long work = (long long)n * p->d.n_layers * (PAGE * ROW / 16);
-  offload_kernel<<<launch_blocks(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p->d, n, d_pool_pages,
-                                                                                             d_host_pages);
-  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  return launch_pdl(offload_kernel, dim3(launch_blocks(work, 256)), dim3(256), 0,
+                    reinterpret_cast<cudaStream_t>(stream), 0, p->d, n, d_pool_pages, d_host_pages);
 }
 
 hs_status hs_get_error(hs_pool* p, hs_status* device_status, hs_stream_t stream) {

@@ -90,6 +90,8 @@ resolve_kernel(Dev D, int group, int step, int n_tok, const int32_t* __restrict_
   __shared__ int s_tot, s_cnt[3], s_bin, s_before, s_min;
   __shared__ uint32_t hbin[RS_HBINS];
 
+  griddep_wait();
+  griddep_launch();
   const int b = blockIdx.x;
   const int K = D.topk;
   if (b >= n_tok) return;
@@ -388,6 +390,8 @@ copy_miss_kernel(Dev D, int group, int n_tok) {
   __shared__ int pre[1025];
   __shared__ int wt[32];
   const int tid = threadIdx.x;
+  griddep_wait();
+  griddep_launch();
   // exclusive prefix of miss_count over the batch (n_tok <= 1024)
   int run = 0;
   for (int base = 0; base < n_tok; base += 256) {
@@ -444,10 +448,10 @@ hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* 
       return HS_ERR_CUDA;
     attr = true;
   }
-  resolve_kernel<<<n, RS_THREADS, RS_SMEM, st>>>(p->d, group, step, n, d_req, d_topk, d_row_ids, d_plan);
-  if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
-  copy_miss_kernel<<<2 * num_sms(), 256, 0, st>>>(p->d, group, n);
-  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  hs_status s = launch_pdl(resolve_kernel, dim3(n), dim3(RS_THREADS), RS_SMEM, st, 0, p->d, group, step, n, d_req,
+                           d_topk, d_row_ids, d_plan);
+  if (s != HS_OK) return s;
+  return launch_pdl(copy_miss_kernel, dim3(2 * num_sms()), dim3(256), 0, st, 0, p->d, group, n);
 }
 
 }  // namespace hs
