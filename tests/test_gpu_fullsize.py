@@ -1,0 +1,71 @@
+"""Parity at the workloads' full sizes, through the C ABI, in the same calls bench.py times.
+
+Bit-exact: top-K sets of every query token, resolver plans (kind, slot, row id,
+evicted token), and the pool bytes behind a seeded sample of row ids; indexer
+scores in full for the 128K workload. Attention: every output within max |err|
+<= 1e-2 and relative L2 <= 5e-3 of the fp64 oracle.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from oracle.engine import OracleRun
+from sparse_mla_kv_indexer_gb300 import schedule as S
+from sparse_mla_kv_indexer_gb300 import workload as W
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+REL_L2 = 5e-3
+
+
+@pytest.mark.parametrize("name,steps,scores", [("ctx128k", 2, True), ("ctx1m", 1, False),
+                                               ("batch32", 1, False), ("multiturn", 1, False)])
+def test_parity_full_size(name, steps, scores):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_mla_kv_indexer_gb300.driver import GpuRun
+    cfg = dataclasses.replace(W.named_config(name), steps=steps)
+    wl = W.Workload(cfg)
+    sch = S.Schedule(cfg)
+    plans = [sch.plan(s) for s in range(steps)]
+    oracle = OracleRun(wl, sch.setup, keep_scores=scores)
+    gpu = GpuRun(wl, sch.setup, keep_scores=scores)
+    rng = np.random.default_rng(0)
+    total_miss = 0
+    try:
+        for plan in plans:
+            o = oracle.step(plan)
+            g = gpu.step(plan)
+            total_miss += sum(len(m) for m in o["misses"])
+            assert g["status"] == 0, f"device status {g['status']}"
+            toks = plan.tokens
+            for grp in range(cfg.n_groups):
+                if scores:
+                    for i, t in enumerate(toks):
+                        assert np.array_equal(g["scores"][grp][i, :t.limit], o["scores"][grp][i])
+                assert np.array_equal(g["topk"][grp], o["topk"][grp]), (plan.step, grp)
+                pg = g["plan"][grp]
+                assert np.array_equal(g["row_ids"][grp], o["row_ids"][grp])
+                assert np.array_equal(pg[..., 0], o["kind"][grp])
+                assert np.array_equal(pg[..., 1], o["slot"][grp])
+                assert np.array_equal(pg[..., 3], o["evicted"][grp])
+                for l in cfg.group_layers(grp):
+                    rows = gpu.kv[l]
+                    for i in rng.choice(len(toks), size=min(8, len(toks)), replace=False):
+                        t = toks[i]
+                        sel = o["topk"][grp][i]
+                        pick = rng.choice(np.nonzero(sel >= 0)[0], size=64, replace=False)
+                        rid = torch.from_numpy(g["row_ids"][grp][i][pick].astype(np.int64)).to(rows.device)
+                        got = rows.view(-1, W.ROW_BYTES)[rid].cpu().numpy()
+                        assert np.array_equal(got, wl.kv_rows(t.req, l)[sel[pick]])
+            for l in range(cfg.n_layers):
+                d = g["o"][l] - o["o"][l]
+                err = np.abs(d).max()
+                rel = np.linalg.norm(d) / np.linalg.norm(o["o"][l])
+                assert err <= ATOL and rel <= REL_L2, (plan.step, l, err, rel)
+        assert gpu.pool.counters().misses == total_miss
+    finally:
+        gpu.close()
