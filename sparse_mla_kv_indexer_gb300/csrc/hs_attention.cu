@@ -5,27 +5,32 @@
 // 576 dims and PV over 512; every row serves all 64 heads (section "PCP: split
 // tokens, not heads"), which is what puts sparse MLA near the compute ridge.
 //
-// One CTA (16 warps) per (query token, block of 128 selected rows):
+// One CTA (16 warps) per (query token, group of HPC heads, block of 128 selected
+// rows); the row-block CTAs of one (token, head group) form a thread-block
+// cluster. HPC is 64 for large batches and 16 or 32 when few query tokens would
+// leave most SMs idle: the head groups then run as independent clusters, which
+// spreads one token over more SMs and shortens every per-CTA phase after the
+// gather (each head group gathers the same rows; the repeats hit L2).
 //  * every thread loads ~10 of the block's 16-byte row chunks at once, gathered by
 //    HMA row id (one stride for resident and hot rows), and puts each chunk in
 //    place: the FP8 latent widened to bf16 by a bit shuffle that is exact up to
 //    the constant factor 2^-120 (normal and subnormal e4m3 alike), the fp32 group
 //    scales to a small table, the bf16 rope unchanged; the 128 x 576 bf16 tile
 //    (128-byte swizzle) is the K-major A operand of QK and the MN-major A
-//    operand of PV; the bf16 query is the B operand unchanged;
+//    operand of PV; the bf16 query is the K-major B operand unchanged;
 //  * QK on tcgen05 into five TMEM accumulators (four 128-dim latent groups and
 //    the rope), so each row's per-group scales (x 2^120) are applied in fp32 when
 //    the scores are read back: s = sum_g scale_g * S_g + S_rope;
-//  * softmax from TMEM: each thread owns one row and 16 heads; per-head max and
-//    sum over rows use a warp transpose-reduction and shared memory;
+//  * softmax from TMEM: each thread owns one row and HPC/4 heads; per-head max
+//    and sum over rows use a warp transpose-reduction and shared memory;
 //  * PV on tcgen05 per latent group g with P_g = p * scale_g * 2^120 (bf16),
 //    so the unscaled FP8 values serve as V;
-//  * the CTAs of one token form a thread-block cluster: they exchange their
-//    per-head (max, sum) through distributed shared memory, each CTA writes its
-//    partial output, scaled by its log-sum-exp weight and rounded to fp16, to a
-//    per-token merge buffer (it stays in L2), and after one cluster barrier each
-//    CTA sums one slice of the 512 output dims over the splits in fp32 and
-//    writes it as bf16.
+//  * the CTAs of one cluster exchange their per-head (max, sum) through
+//    distributed shared memory, each writes its partial output, scaled by its
+//    log-sum-exp weight and rounded to fp16, to a per-token merge buffer (it stays
+//    in L2), and after one cluster barrier each CTA sums one slice of the 512
+//    output dims over the splits in fp32, transposes it through shared memory and
+//    writes it as bf16 in 16-byte pieces.
 // Per-group scales must stay below 256 (so scale * 2^120 fits fp32 and bf16).
 #include "hs_internal.cuh"
 
@@ -33,19 +38,26 @@ namespace hs {
 
 constexpr int AT_THREADS = 512;
 constexpr int AT_KV_COL = ATTN_ROWS * 128;       // 16 KB: one 64-dim bf16 atom column of the tile
-constexpr int AT_Q_COL = 64 * 128;               // 8 KB: one atom column of Q (<= 64 heads)
-constexpr int AT_P_COL = ATTN_ROWS * 128;        // 16 KB: one P_g matrix [128 rows][64 heads] bf16
 constexpr int AT_OFF_KV = 0;
-constexpr int AT_OFF_Q = 9 * AT_KV_COL;          // 144 KB; after QK the region holds P_0..P_3
-constexpr int AT_OFF_MISC = AT_OFF_Q + 9 * AT_Q_COL;   // 216 KB
+constexpr int AT_OFF_Q = 9 * AT_KV_COL;          // 144 KB; after QK the query region holds P_0..P_3
 constexpr int AT_MISC = 6144;
-constexpr int AT_SMEM = AT_OFF_MISC + AT_MISC + 1024;
 constexpr int AT_CHUNKS = ATTN_ROWS * ROW_CHUNKS;        // 5,248 16-byte chunks per block
 constexpr int AT_CPT = (AT_CHUNKS + AT_THREADS - 1) / AT_THREADS;   // 11 per thread
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float TWO_POW_120 = 1.329227995784916e36f;
-static_assert(4 * AT_P_COL <= 9 * AT_Q_COL, "P_0..P_3 fit in the query region");
-static_assert(AT_SMEM <= 232448, "shared memory budget");
+
+// Shared-memory plan for HPC heads per CTA.
+template <int HPC>
+struct AtPlan {
+  static constexpr int Q_COL = HPC * 128;                 // one 64-dim atom column of Q [HPC][576]
+  static constexpr int P_G = 2 * HPC * 128;               // one P_g [HPC heads][128 rows] bf16
+  static constexpr int OFF_MISC = AT_OFF_Q + 9 * Q_COL;
+  static constexpr int SMEM = OFF_MISC + AT_MISC + 1024;
+  static constexpr int HW = HPC / 4;                      // heads per warp in the softmax
+  static_assert(4 * P_G <= 9 * Q_COL, "P_0..P_3 fit in the query region");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(HPC * 512 * 4 <= 9 * AT_KV_COL, "the merge transpose fits in the KV region");
+};
 
 // Four e4m3 bytes -> four bf16 values times 2^-120 (exact for every finite code):
 // the e4m3 exponent/mantissa bits land on the bf16 exponent/mantissa fields.
@@ -62,23 +74,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float x, float y) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// After the call lanes l and l ^ 16 hold op-reduction over all 32 lanes of v[l & 15].
-template <bool MAX>
-__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16]) {
+// Reduces each of the HW values over the 32 lanes of the warp; afterwards lane l
+// holds the reduction of v[l % HW]. The first log2(HW) steps exchange half of the
+// values with the partner lane (a transpose), the rest are plain butterflies.
+template <int HW, bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[HW]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int o = 8; o >= 1; o >>= 1) {
+  for (int o = HW / 2; o >= 1; o >>= 1) {
     const bool hi = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < o; ++i) {
-      float send = hi ? v[i] : v[i + o];
-      float keep = hi ? v[i + o] : v[i];
-      float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      const float send = hi ? v[i] : v[i + o];
+      const float keep = hi ? v[i + o] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
       v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
-  return MAX ? fmaxf(v[0], other) : v[0] + other;
+#pragma unroll
+  for (int o = HW; o < 32; o <<= 1) {
+    const float other = __shfl_xor_sync(0xffffffffu, v[0], o);
+    v[0] = MAX ? fmaxf(v[0], other) : v[0] + other;
+  }
+  return v[0];
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -92,30 +110,33 @@ __device__ __forceinline__ uint32_t cluster_size() {
   return r;
 }
 
+template <int HPC>
 __global__ void __launch_bounds__(AT_THREADS, 1)
 attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t* __restrict__ row_ids,
                  float scale_log2, uint16_t* __restrict__ out, float* __restrict__ lse_out) {
+  using PL = AtPlan<HPC>;
+  constexpr int HW = PL::HW;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* KV = smem + AT_OFF_KV;
   uint8_t* Qs = smem + AT_OFF_Q;
   uint8_t* Ps = smem + AT_OFF_Q;                                             // P_g after QK
-  int32_t* ids = reinterpret_cast<int32_t*>(smem + AT_OFF_MISC);            // [128]
+  int32_t* ids = reinterpret_cast<int32_t*>(smem + PL::OFF_MISC);           // [128]
   float4* scl = reinterpret_cast<float4*>(ids + ATTN_ROWS);                  // [128] group scales
-  float* red = reinterpret_cast<float*>(scl + ATTN_ROWS);                    // [4][64]
-  float* mfin = red + 4 * 64;                                                // [64] this split's max (log2 units)
-  float* lfin = mfin + 64;                                                   // [64] this split's sum
-  float* wmine = lfin + 64;                                                  // [64] weight of this split
-  float* gstat = wmine + 64;                                                 // [64] lse
-  uint64_t* bar = reinterpret_cast<uint64_t*>(gstat + 64);                   // [1] MMA completion
+  float* red = reinterpret_cast<float*>(scl + ATTN_ROWS);                    // [4][HPC]
+  float* mfin = red + 4 * HPC;                                               // [HPC] this split's max (log2 units)
+  float* lfin = mfin + HPC;                                                  // [HPC] this split's sum
+  float* wmine = lfin + HPC;                                                 // [HPC] weight of this split
+  float* gstat = wmine + HPC;                                                // [HPC] lse
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gstat + HPC);                  // [1] MMA completion
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
-  int32_t* s_flag = reinterpret_cast<int32_t*>(tslot + 1);
 
   const uint32_t split = cluster_rank();
   const uint32_t n_splits = cluster_size();
-  const int tok = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = D.n_heads, K = D.topk;
+  const int n_hgrp = H / HPC;
+  const int tok = blockIdx.y / n_hgrp, hgrp = blockIdx.y - tok * n_hgrp;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint8_t* kv = D.kv[layer];
   const long long max_row = (long long)D.num_pages * PAGE;
 
@@ -123,7 +144,6 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   if (tid == 0) {
     mbar_init(smem_u32(bar), 1);
     fence_mbar_init();
-    *s_flag = 0;
   }
   griddep_wait();
   griddep_launch();
@@ -133,14 +153,14 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     if (id >= max_row) { set_status(D.status, HS_ERR_BAD_ID); id = -1; }
     ids[tid] = id;
   }
-  // ---- Q: [H, 576] bf16, 72 chunks of 8 per head, loads in flight ----
-  const uint16_t* qt = q + (size_t)tok * H * QK;
-  constexpr int QPT = 64 * 72 / AT_THREADS;   // 9 chunks per thread at 64 heads
+  // ---- Q: this head group's [HPC, 576] bf16, 72 chunks of 8 per head, loads in flight ----
+  const uint16_t* qt = q + ((size_t)tok * H + (size_t)hgrp * HPC) * QK;
+  constexpr int QPT = (HPC * 72 + AT_THREADS - 1) / AT_THREADS;
   uint4 qv[QPT];
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
     const int c = tid + k * AT_THREADS;
-    qv[k] = c < H * 72 ? __ldg(reinterpret_cast<const uint4*>(qt) + c) : make_uint4(0, 0, 0, 0);
+    qv[k] = c < HPC * 72 ? __ldg(reinterpret_cast<const uint4*>(qt) + c) : make_uint4(0, 0, 0, 0);
   }
   __syncthreads();   // ids ready
   // ---- all row chunks in flight at once: chunk c = row * 41 + part ----
@@ -158,9 +178,9 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
     const int c = tid + k * AT_THREADS;
-    if (c < H * 72) {
+    if (c < HPC * 72) {
       const int h = c / 72, ch = c - h * 72;
-      *reinterpret_cast<uint4*>(Qs + (ch >> 3) * AT_Q_COL + sw128_chunk(h, ch & 7)) = qv[k];
+      *reinterpret_cast<uint4*>(Qs + (ch >> 3) * PL::Q_COL + sw128_chunk(h, ch & 7)) = qv[k];
     }
   }
 #pragma unroll
@@ -188,106 +208,134 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  bool ok = true;
 
-  // ---- S_g^T = KV_g . Q_g^T (g = 0..3 latent groups, 4 = rope): M = 128 rows, N = H ----
+  // ---- S_g^T = KV_g . Q_g^T (g = 0..3 latent groups, 4 = rope): M = 128 rows, N = HPC ----
   if (tid == 0) {
-    const uint32_t idesc = idesc_f16(128, H, false, false, true);
+    const uint32_t idesc = idesc_f16(128, HPC, false, false, true);
     const uint32_t a0 = smem_u32(KV), b0 = smem_u32(Qs);
 #pragma unroll 4
     for (int kk = 0; kk < 36; ++kk) {
       const int g = kk >> 3;          // 8 k-steps of 16 dims per 128-dim group; rope is g = 4
       const uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * AT_KV_COL + (kk & 3) * 32, 16, 1024);
-      const uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * AT_Q_COL + (kk & 3) * 32, 16, 1024);
+      const uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * PL::Q_COL + (kk & 3) * 32, 16, 1024);
       umma_f16(tmem + g * 64, ad, bd, idesc, (kk & 7) != 0);
     }
     umma_commit(smem_u32(bar));
   }
-  if (!mbar_wait(smem_u32(bar), 0, D.status)) *s_flag = 1;
+  ok &= mbar_wait(smem_u32(bar), 0, D.status);
   tc_fence_after();
 
-  // ---- softmax over the 128 rows, per head: warp (row quadrant, head quarter) ----
-  const int quad = warp & 3, hq = warp >> 2;
+  // ---- softmax over the 128 rows, per head: warp (row quadrant, HW-head quarter) ----
+  const int quad = warp & 3, sub = warp >> 2;
   const int row = quad * 32 + lane;
   const bool valid = ids[row] >= 0;
-  const bool active = hq * 16 < H;          // warp-uniform
   const float4 sc4 = scl[row];
   const float sg[4] = {sc4.x * TWO_POW_120, sc4.y * TWO_POW_120, sc4.z * TWO_POW_120, sc4.w * TWO_POW_120};
-  float z[16];
-  if (active) {
-    const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(hq * 16);
-    uint32_t r[16];
-    tmem_ld16(ta + 256, r);         // rope part
+  float z[HW];
+  {
+    const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(sub * HW);
+    // rope part and the four groups in one wave (two waves at 16 heads per warp, for registers)
+    constexpr int WAVE = HW >= 16 ? 2 : 4;
+    uint32_t r[WAVE + 1][HW];
+    tmem_ld_cols<HW>(ta + 256, r[WAVE]);
+#pragma unroll
+    for (int g = 0; g < WAVE; ++g) tmem_ld_cols<HW>(ta + g * 64, r[g]);
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < HW; ++i) {
+      float acc = __uint_as_float(r[WAVE][i]);
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      tmem_ld16(ta + g * 64, r);
+      for (int g = 0; g < WAVE; ++g) acc = fmaf(__uint_as_float(r[g][i]), sg[g], acc);
+      z[i] = acc;
+    }
+    if constexpr (WAVE < 4) {
+#pragma unroll
+      for (int g = WAVE; g < 4; ++g) tmem_ld_cols<HW>(ta + g * 64, r[g - WAVE]);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = fmaf(__uint_as_float(r[i]), sg[g], z[i]);
+      for (int i = 0; i < HW; ++i)
+#pragma unroll
+        for (int g = WAVE; g < 4; ++g) z[i] = fmaf(__uint_as_float(r[g - WAVE][i]), sg[g], z[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z[i] = valid ? z[i] * scale_log2 : -INFINITY;
-    float t[16];
+    for (int i = 0; i < HW; ++i) z[i] = valid ? z[i] * scale_log2 : -INFINITY;
+    float t[HW];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) t[i] = z[i];
-    const float m = warp_transpose_reduce16<true>(t);
-    if (lane < 16) red[quad * 64 + hq * 16 + lane] = m;
+    for (int i = 0; i < HW; ++i) t[i] = z[i];
+    const float m = warp_transpose_reduce<HW, true>(t);
+    if (lane < HW) red[quad * HPC + sub * HW + lane] = m;
   }
   __syncthreads();
-  if (tid < H) mfin[tid] = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+  if (tid < HPC) mfin[tid] = fmaxf(fmaxf(red[tid], red[HPC + tid]), fmaxf(red[2 * HPC + tid], red[3 * HPC + tid]));
   __syncthreads();
-  if (active) {
-    float t[16];
+  {
+    float t[HW];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float m = mfin[hq * 16 + i];
+    for (int i = 0; i < HW; ++i) {
+      const float m = mfin[sub * HW + i];
       const float p = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
       z[i] = p;
       t[i] = p;
     }
-    const float l = warp_transpose_reduce16<false>(t);
-    if (lane < 16) red[quad * 64 + hq * 16 + lane] = l;
-    // P_g^T[row][head] = p * scale_g * 2^120 (bf16), the MN-major B operand of group g
+    const float l = warp_transpose_reduce<HW, false>(t);
+    if (lane < HW) red[quad * HPC + sub * HW + lane] = l;
+    // P_g = p * scale_g * 2^120 (bf16), the B operand of group g's PV. At 64 heads
+    // it is MN-major, P_g^T[row][head] with one 128-byte line per row (16-byte
+    // stores); below that a line would be shorter than the swizzle atom, so it is
+    // K-major, P_g[head][row], written element by element.
+    if constexpr (HPC == 64) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint8_t* pg = Ps + g * AT_P_COL;
+      for (int g = 0; g < 4; ++g) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float* zz = z + 8 * c;
-        *reinterpret_cast<uint4*>(pg + sw128_chunk(row, hq * 2 + c)) =
-            make_uint4(pack_bf16x2(zz[0] * sg[g], zz[1] * sg[g]), pack_bf16x2(zz[2] * sg[g], zz[3] * sg[g]),
-                       pack_bf16x2(zz[4] * sg[g], zz[5] * sg[g]), pack_bf16x2(zz[6] * sg[g], zz[7] * sg[g]));
+        for (int c = 0; c < HW / 8; ++c) {
+          const float* zz = z + 8 * c;
+          *reinterpret_cast<uint4*>(Ps + g * PL::P_G + sw128_chunk(row, sub * (HW / 8) + c)) =
+              make_uint4(pack_bf16x2(zz[0] * sg[g], zz[1] * sg[g]), pack_bf16x2(zz[2] * sg[g], zz[3] * sg[g]),
+                         pack_bf16x2(zz[4] * sg[g], zz[5] * sg[g]), pack_bf16x2(zz[6] * sg[g], zz[7] * sg[g]));
+        }
+      }
+    } else {
+      uint16_t* pbase = reinterpret_cast<uint16_t*>(Ps + (row >> 6) * (HPC * 128));
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+#pragma unroll
+        for (int i = 0; i < HW; ++i) {
+          const int h = sub * HW + i;
+          pbase[(g * PL::P_G + sw128_off(h, row & 63)) >> 1] = __bfloat16_as_ushort(__float2bfloat16_rn(z[i] * sg[g]));
+        }
       }
     }
   }
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();   // every S read: the accumulators may be overwritten by PV
-  if (tid < H) lfin[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+  if (tid < HPC) lfin[tid] = red[tid] + red[HPC + tid] + red[2 * HPC + tid] + red[3 * HPC + tid];
   tc_fence_after();
 
-  // ---- O_g^T = V_g^T . P_g^T : M = 128 latent dims, N = H, K = 128 rows ----
+  // ---- O_g^T = V_g^T . P_g^T : M = 128 latent dims, N = HPC, K = 128 rows ----
   if (tid == 0) {
-    const uint32_t idesc = idesc_f16(128, H, true, true, true);
+    constexpr bool P_MN = HPC == 64;
+    const uint32_t idesc = idesc_f16(128, HPC, true, P_MN, true);
     const uint32_t kv0 = smem_u32(KV), p0 = smem_u32(Ps);
     for (int g = 0; g < 4; ++g) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t ad = smem_desc_sw128(kv0 + (2 * g) * AT_KV_COL + kk * 2048, AT_KV_COL, 1024);
-        const uint64_t bd = smem_desc_sw128(p0 + g * AT_P_COL + kk * 2048, AT_P_COL, 1024);
+        const uint64_t bd =
+            P_MN ? smem_desc_sw128(p0 + g * PL::P_G + kk * 2048, PL::P_G, 1024)
+                 : smem_desc_sw128(p0 + g * PL::P_G + (kk >> 2) * (HPC * 128) + (kk & 3) * 32, 16, 1024);
         umma_f16(tmem + g * 64, ad, bd, idesc, kk > 0);
       }
     }
     umma_commit(smem_u32(bar));
   }
-  if (!mbar_wait(smem_u32(bar), 1, D.status)) *s_flag = 1;
+  ok &= mbar_wait(smem_u32(bar), 1, D.status);
   tc_fence_after();
   // every CTA's (max, sum) is published
   cluster_sync();
   // ---- cluster-wide log-sum-exp weight of this split, per head ----
-  if (tid < H) {
+  if (tid < HPC) {
     float ms[MAX_SPLITS], ls[MAX_SPLITS];
 #pragma unroll
     for (int s = 0; s < MAX_SPLITS; ++s) {          // all remote loads in flight at once
@@ -307,79 +355,111 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   }
   __syncthreads();
 
-  // ---- weighted partial O (fp16) to the token's merge buffer in global memory ----
-  // layout [split][dim][head] (fp16); the cluster barrier below orders these
-  // writes before the other CTAs of the cluster read them (cluster scope)
-  __half* part = D.o_part + (size_t)tok * MAX_SPLITS * 512 * 64;
-  if (active) {
-    float wv[16];
+  // ---- weighted partial O (fp16) to the merge buffer: warp (row quadrant, group) ----
+  // layout per (token, head group): [split][dim][HPC] fp16; the cluster barrier
+  // below orders these writes before the other CTAs of the cluster read them
+  __half* part = D.o_part + (size_t)tok * MAX_SPLITS * 512 * 64 + (size_t)hgrp * MAX_SPLITS * 512 * HPC;
+  {
+    const int g = sub;
+    const int dim = g * 128 + quad * 32 + lane;
+    constexpr int CW = HPC < 32 ? HPC : 32;   // columns per TMEM read
+    uint4* dst = reinterpret_cast<uint4*>(part + ((size_t)split * 512 + dim) * HPC);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) wv[i] = wmine[hq * 16 + i];
-    for (int g = 0; g < 4; ++g) {
-      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 64 + hq * 16);
-      const int dim = g * 128 + quad * 32 + lane;
-      uint32_t r[16];
-      tmem_ld16(ta, r);
+    for (int h0 = 0; h0 < HPC; h0 += CW) {
+      uint32_t r[CW];
+      tmem_ld_cols<CW>(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 64 + h0), r);
       tmem_wait_ld();
-      uint32_t hv[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        __half2 h2 = __floats2half2_rn(__uint_as_float(r[2 * i]) * wv[2 * i],
-                                       __uint_as_float(r[2 * i + 1]) * wv[2 * i + 1]);
-        hv[i] = *reinterpret_cast<uint32_t*>(&h2);
+      for (int c = 0; c < CW / 8; ++c) {
+        uint32_t hv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = c * 8 + 2 * i;
+          __half2 h2 = __floats2half2_rn(__uint_as_float(r[h]) * wmine[h0 + h],
+                                         __uint_as_float(r[h + 1]) * wmine[h0 + h + 1]);
+          hv[i] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        dst[(h0 >> 3) + c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
       }
-      uint4* dst = reinterpret_cast<uint4*>(part + ((size_t)split * 512 + dim) * 64 + hq * 16);
-      dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-      dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
     }
   }
   tc_fence_before();
   cluster_sync();   // every partial output written
-  // ---- this CTA sums one slice of the 512 dims over the splits and writes bf16 ----
+  // ---- this CTA sums one slice of the 512 dims over the splits, transposes, writes bf16 ----
   {
-    const int slice = ((512 / (int)n_splits) + 3) & ~3;
+    const int slice = ((512 / (int)n_splits) + 7) & ~7;
     const int d_lo = min(512, (int)split * slice), d_hi = min(512, d_lo + slice);
     const int nd = d_hi - d_lo;
-    for (int e = tid; e < nd * (H / 8); e += AT_THREADS) {
-      const int dd = e / (H / 8), h8 = e - dd * (H / 8);
+    float* tr = reinterpret_cast<float*>(KV);      // [HPC][slice] fp32; the KV tile is no longer read
+    for (int e = tid; e < nd * (HPC / 8); e += AT_THREADS) {
+      const int dd = e / (HPC / 8), h8 = e - dd * (HPC / 8);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint4 v[MAX_SPLITS];
+      constexpr int SB = MAX_SPLITS;   // loads in flight per batch
 #pragma unroll
-      for (int s = 0; s < MAX_SPLITS; ++s)   // coherent loads: written during this kernel
-        v[s] = s < (int)n_splits ? ld_cg_v4(part + ((size_t)s * 512 + d_lo + dd) * 64 + h8 * 8)
-                                 : make_uint4(0, 0, 0, 0);
+      for (int s0 = 0; s0 < MAX_SPLITS; s0 += SB) {
+        uint4 v[SB];
 #pragma unroll
-      for (int s = 0; s < MAX_SPLITS; ++s) {
-        const uint32_t w[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
+        for (int s = 0; s < SB; ++s)   // coherent loads: written during this kernel
+          v[s] = s0 + s < (int)n_splits ? ld_cg_v4(part + ((size_t)(s0 + s) * 512 + d_lo + dd) * HPC + h8 * 8)
+                                        : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-          acc[2 * k] += f.x;
-          acc[2 * k + 1] += f.y;
+        for (int s = 0; s < SB; ++s) {
+          const uint32_t w[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+            acc[2 * k] += f.x;
+            acc[2 * k + 1] += f.y;
+          }
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        out[((size_t)tok * H + h8 * 8 + j) * 512 + d_lo + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+      for (int j = 0; j < 8; ++j) tr[(h8 * 8 + j) * slice + dd] = acc[j];
     }
-    if (split == 0 && lse_out && tid < H) lse_out[(size_t)tok * H + tid] = gstat[tid];
+    __syncthreads();
+    const int nc = nd >> 3;
+    for (int e = tid; e < HPC * nc; e += AT_THREADS) {
+      const int h = e / nc, c = e - h * nc;
+      const float* src = tr + h * slice + c * 8;
+      *reinterpret_cast<uint4*>(out + ((size_t)tok * H + (size_t)hgrp * HPC + h) * 512 + d_lo + c * 8) =
+          make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]), pack_bf16x2(src[4], src[5]),
+                     pack_bf16x2(src[6], src[7]));
+    }
+    if (split == 0 && lse_out && tid < HPC) lse_out[(size_t)tok * H + (size_t)hgrp * HPC + tid] = gstat[tid];
   }
+  (void)ok;
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows, float sm_scale,
-                           uint16_t* d_out, float* d_lse, cudaStream_t st) {
+template <int HPC>
+static hs_status launch_attention_hpc(hs_pool* p, int layer, int n, int n_splits, const uint16_t* d_q,
+                                      const int32_t* d_rows, float scale_log2, uint16_t* d_out, float* d_lse,
+                                      cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    if (cudaFuncSetAttribute(attention_kernel<HPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AtPlan<HPC>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(attention_kernel<HPC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return HS_ERR_CUDA;
     attr = true;
   }
+  const int n_hgrp = p->cfg.n_heads / HPC;
+  return launch_pdl(attention_kernel<HPC>, dim3(n_splits, n * n_hgrp, 1), dim3(AT_THREADS, 1, 1), AtPlan<HPC>::SMEM,
+                    st, n_splits, p->d, layer, d_q, d_rows, scale_log2, d_out, d_lse);
+}
+
+hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows, float sm_scale,
+                           uint16_t* d_out, float* d_lse, cudaStream_t st) {
   const int n_splits = (p->cfg.topk + ATTN_ROWS - 1) / ATTN_ROWS;
-  return launch_pdl(attention_kernel, dim3(n_splits, n, 1), dim3(AT_THREADS, 1, 1), AT_SMEM, st, n_splits, p->d, layer,
-                    d_q, d_rows, sm_scale * LOG2E, d_out, d_lse);
+  const int H = p->cfg.n_heads;
+  // fewer heads per CTA while the head groups still fit on the SMs side by side
+  int hpc = H < 64 ? H : 64;
+  while (hpc > 16 && (long long)n * n_splits * (H / (hpc / 2)) <= num_sms()) hpc /= 2;
+  const float sl = sm_scale * LOG2E;
+  if (hpc == 16) return launch_attention_hpc<16>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
+  if (hpc == 32) return launch_attention_hpc<32>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
+  return launch_attention_hpc<64>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
 }
 
 }  // namespace hs

@@ -190,6 +190,33 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[15])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+// N consecutive fp32 columns (N = 4, 8, 16, 32 or 64) of the thread's own lane,
+// issued without waiting; the caller waits once with tmem_wait_ld().
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  static_assert(N == 4 || N == 8 || N == 16 || N == 32 || N == 64, "column count");
+  if constexpr (N == 4) {
+    tmem_ld4(taddr, r);
+  } else if constexpr (N == 8) {
+    tmem_ld8(taddr, r);
+  } else if constexpr (N == 16) {
+    tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
+  } else {
+#pragma unroll
+    for (int j = 0; j < N / 32; ++j) tmem_ld32(taddr + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * j));
+  }
+}
 
 // Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
 //  K-major operand: rows of 128 B (64 16-bit elements), 8-row groups `sbo` apart.
