@@ -25,12 +25,13 @@
 //    and sum over rows use a warp transpose-reduction and shared memory;
 //  * PV on tcgen05 per latent group g with P_g = p * scale_g * 2^120 (bf16),
 //    so the unscaled FP8 values serve as V;
-//  * the CTAs of one cluster exchange their per-head (max, sum) through
-//    distributed shared memory, each writes its partial output, scaled by its
-//    log-sum-exp weight and rounded to fp16, to a per-token merge buffer (it stays
-//    in L2), and after one cluster barrier each CTA sums one slice of the 512
-//    output dims over the splits in fp32, transposes it through shared memory and
-//    writes it as bf16 in 16-byte pieces.
+//  * split merge with one cluster barrier: while PV runs, each CTA writes its
+//    per-head (max, sum) to the token's merge record; after PV it writes its
+//    partial output, normalised by its own sum and rounded to fp16, to a
+//    per-token merge buffer (both stay in L2). After the barrier each CTA turns
+//    the (max, sum) of all splits into log-sum-exp weights (a 16-lane group per
+//    head), sums one slice of the 512 output dims over the splits in fp32,
+//    transposes it through shared memory and writes it as bf16 in 16-byte pieces.
 // Per-group scales must stay below 256 (so scale * 2^120 fits fp32 and bf16).
 #include "hs_internal.cuh"
 
@@ -56,7 +57,7 @@ struct AtPlan {
   static constexpr int HW = HPC / 4;                      // heads per warp in the softmax
   static_assert(4 * P_G <= 9 * Q_COL, "P_0..P_3 fit in the query region");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(HPC * 512 * 4 <= 9 * AT_KV_COL, "the merge transpose fits in the KV region");
+  static_assert(HPC * 512 * 4 + MAX_SPLITS * HPC * 4 <= 9 * AT_KV_COL, "merge scratch fits in the KV region");
 };
 
 // Four e4m3 bytes -> four bf16 values times 2^-120 (exact for every finite code):
@@ -128,8 +129,8 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   float* lfin = mfin + HPC;                                                  // [HPC] this split's sum
   float* wmine = lfin + HPC;                                                 // [HPC] weight of this split
   float* gstat = wmine + HPC;                                                // [HPC] lse
-  uint64_t* bar = reinterpret_cast<uint64_t*>(gstat + HPC);                  // [1] MMA completion
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gstat + HPC);                  // [2] QK, PV completion
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
 
   const uint32_t split = cluster_rank();
   const uint32_t n_splits = cluster_size();
@@ -142,7 +143,8 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
 
   if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
   if (tid == 0) {
-    mbar_init(smem_u32(bar), 1);
+    mbar_init(smem_u32(bar), 5);       // one arrival per QK accumulator
+    mbar_init(smem_u32(bar + 1), 4);   // one arrival per PV group
     fence_mbar_init();
   }
   griddep_wait();
@@ -211,15 +213,18 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   bool ok = true;
 
   // ---- S_g^T = KV_g . Q_g^T (g = 0..3 latent groups, 4 = rope): M = 128 rows, N = HPC ----
-  if (tid == 0) {
+  // One issuing thread per accumulator (warp g, lane 0): at small N the MMAs are
+  // short and the issue itself is the cost, so five threads issue side by side.
+  if (lane == 0 && warp < 5) {
+    const int g = warp;
     const uint32_t idesc = idesc_f16(128, HPC, false, false, true);
     const uint32_t a0 = smem_u32(KV), b0 = smem_u32(Qs);
+    const int k0 = g * 8, k1 = g < 4 ? k0 + 8 : 36;   // 8 k-steps of 16 dims per group, 4 for the rope
 #pragma unroll 4
-    for (int kk = 0; kk < 36; ++kk) {
-      const int g = kk >> 3;          // 8 k-steps of 16 dims per 128-dim group; rope is g = 4
+    for (int kk = k0; kk < k1; ++kk) {
       const uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * AT_KV_COL + (kk & 3) * 32, 16, 1024);
       const uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * PL::Q_COL + (kk & 3) * 32, 16, 1024);
-      umma_f16(tmem + g * 64, ad, bd, idesc, (kk & 7) != 0);
+      umma_f16(tmem + g * 64, ad, bd, idesc, kk != k0);
     }
     umma_commit(smem_u32(bar));
   }
@@ -310,54 +315,38 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();   // every S read: the accumulators may be overwritten by PV
-  if (tid < HPC) lfin[tid] = red[tid] + red[HPC + tid] + red[2 * HPC + tid] + red[3 * HPC + tid];
   tc_fence_after();
 
-  // ---- O_g^T = V_g^T . P_g^T : M = 128 latent dims, N = HPC, K = 128 rows ----
-  if (tid == 0) {
+  // ---- O_g^T = V_g^T . P_g^T : M = 128 latent dims, N = HPC, K = 128 rows (warp g issues) ----
+  if (lane == 0 && warp < 4) {
+    const int g = warp;
     constexpr bool P_MN = HPC == 64;
     const uint32_t idesc = idesc_f16(128, HPC, true, P_MN, true);
     const uint32_t kv0 = smem_u32(KV), p0 = smem_u32(Ps);
-    for (int g = 0; g < 4; ++g) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc_sw128(kv0 + (2 * g) * AT_KV_COL + kk * 2048, AT_KV_COL, 1024);
-        const uint64_t bd =
-            P_MN ? smem_desc_sw128(p0 + g * PL::P_G + kk * 2048, PL::P_G, 1024)
-                 : smem_desc_sw128(p0 + g * PL::P_G + (kk >> 2) * (HPC * 128) + (kk & 3) * 32, 16, 1024);
-        umma_f16(tmem + g * 64, ad, bd, idesc, kk > 0);
-      }
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t ad = smem_desc_sw128(kv0 + (2 * g) * AT_KV_COL + kk * 2048, AT_KV_COL, 1024);
+      const uint64_t bd =
+          P_MN ? smem_desc_sw128(p0 + g * PL::P_G + kk * 2048, PL::P_G, 1024)
+               : smem_desc_sw128(p0 + g * PL::P_G + (kk >> 2) * (HPC * 128) + (kk & 3) * 32, 16, 1024);
+      umma_f16(tmem + g * 64, ad, bd, idesc, kk > 0);
     }
-    umma_commit(smem_u32(bar));
+    umma_commit(smem_u32(bar + 1));
   }
-  ok &= mbar_wait(smem_u32(bar), 1, D.status);
+  // while PV runs: this split's per-head (max, sum) to the token's merge record
+  float2* stats = D.o_stats + (size_t)tok * MAX_SPLITS * 64;          // [split][64 heads]
+  if (tid >= 128 && tid < 128 + HPC) {
+    const int h = tid - 128;
+    const float l = red[h] + red[HPC + h] + red[2 * HPC + h] + red[3 * HPC + h];
+    lfin[h] = l;
+    stats[(size_t)split * 64 + hgrp * HPC + h] = make_float2(mfin[h], l);
+  }
+  ok &= mbar_wait(smem_u32(bar + 1), 0, D.status);
   tc_fence_after();
-  // every CTA's (max, sum) is published
-  cluster_sync();
-  // ---- cluster-wide log-sum-exp weight of this split, per head ----
-  if (tid < HPC) {
-    float ms[MAX_SPLITS], ls[MAX_SPLITS];
-#pragma unroll
-    for (int s = 0; s < MAX_SPLITS; ++s) {          // all remote loads in flight at once
-      ms[s] = s < (int)n_splits ? __uint_as_float(ld_cluster_u32(mapa(smem_u32(mfin + tid), s))) : -INFINITY;
-      ls[s] = s < (int)n_splits ? __uint_as_float(ld_cluster_u32(mapa(smem_u32(lfin + tid), s))) : 0.f;
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < MAX_SPLITS; ++s) M = fmaxf(M, ms[s]);
-    float L = 0.f;
-#pragma unroll
-    for (int s = 0; s < MAX_SPLITS; ++s)
-      if (ms[s] != -INFINITY) L += exp2f(ms[s] - M) * ls[s];
-    const float mine = mfin[tid];
-    wmine[tid] = (L > 0.f && mine != -INFINITY) ? exp2f(mine - M) / L : 0.f;
-    gstat[tid] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-  }
-  __syncthreads();
+  __syncthreads();   // lfin
 
-  // ---- weighted partial O (fp16) to the merge buffer: warp (row quadrant, group) ----
-  // layout per (token, head group): [split][dim][HPC] fp16; the cluster barrier
-  // below orders these writes before the other CTAs of the cluster read them
+  // ---- the split's partial O, normalised by its own sum, in fp16 to the merge buffer ----
+  // layout per (token, head group): [split][dim][HPC]; warp (row quadrant, group g)
   __half* part = D.o_part + (size_t)tok * MAX_SPLITS * 512 * 64 + (size_t)hgrp * MAX_SPLITS * 512 * HPC;
   {
     const int g = sub;
@@ -374,48 +363,80 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
         uint32_t hv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int h = c * 8 + 2 * i;
-          __half2 h2 = __floats2half2_rn(__uint_as_float(r[h]) * wmine[h0 + h],
-                                         __uint_as_float(r[h + 1]) * wmine[h0 + h + 1]);
+          const int h = h0 + c * 8 + 2 * i;
+          const float i0 = lfin[h] > 0.f ? 1.f / lfin[h] : 0.f, i1 = lfin[h + 1] > 0.f ? 1.f / lfin[h + 1] : 0.f;
+          __half2 h2 = __floats2half2_rn(__uint_as_float(r[h - h0]) * i0, __uint_as_float(r[h - h0 + 1]) * i1);
           hv[i] = *reinterpret_cast<uint32_t*>(&h2);
         }
         dst[(h0 >> 3) + c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
       }
     }
   }
+  // one cluster barrier: every split's (max, sum) and partial are written (cluster scope)
   tc_fence_before();
-  cluster_sync();   // every partial output written
-  // ---- this CTA sums one slice of the 512 dims over the splits, transposes, writes bf16 ----
+  cluster_arrive_release();
+  cluster_wait_acquire();
+
+  // ---- this CTA's slice of the 512 dims: the partials are loaded first, so their
+  //      round trip to L2 overlaps the one for the (max, sum) of the splits ----
+  const int slice = ((512 + (int)n_splits - 1) / (int)n_splits + 7) & ~7;
+  const int d_lo = min(512, (int)split * slice), d_hi = min(512, d_lo + slice);
+  const int nd = d_hi - d_lo;
+  float* wts = reinterpret_cast<float*>(KV);            // [MAX_SPLITS][HPC]; the KV tile is no longer read
+  float* tr = wts + MAX_SPLITS * HPC;                    // [HPC][slice] fp32 transpose
   {
-    const int slice = ((512 / (int)n_splits) + 7) & ~7;
-    const int d_lo = min(512, (int)split * slice), d_hi = min(512, d_lo + slice);
-    const int nd = d_hi - d_lo;
-    float* tr = reinterpret_cast<float*>(KV);      // [HPC][slice] fp32; the KV tile is no longer read
-    for (int e = tid; e < nd * (HPC / 8); e += AT_THREADS) {
+    // items (dim, 8 heads); a thread's first item is loaded before the weights are known
+    const int n_items = nd * (HPC / 8);
+    uint4 v[MAX_SPLITS];
+    auto load_item = [&](int e) {
+      const int dd = e / (HPC / 8), h8 = e - dd * (HPC / 8);
+#pragma unroll
+      for (int sp = 0; sp < MAX_SPLITS; ++sp)   // coherent loads: written during this kernel
+        v[sp] = sp < (int)n_splits ? ld_cg_v4(part + ((size_t)sp * 512 + d_lo + dd) * HPC + h8 * 8)
+                                   : make_uint4(0, 0, 0, 0);
+    };
+    if (tid < n_items) load_item(tid);
+    // weights of the splits per head: a 16-lane group per head, one lane per split
+    for (int t0 = 0; t0 < MAX_SPLITS * HPC; t0 += AT_THREADS) {
+      const int t = t0 + tid;
+      if (t0 + (tid & ~31) < MAX_SPLITS * HPC) {           // whole warps only: shuffles below
+        const int h = t >> 4, sp = t & 15;
+        const float2 ml = sp < (int)n_splits ? ld_cg_f2(stats + (size_t)sp * 64 + hgrp * HPC + h)
+                                             : make_float2(-INFINITY, 0.f);
+        float M = ml.x;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float e = ml.x == -INFINITY ? 0.f : ml.y * exp2f(ml.x - M);
+        float L = e;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        wts[sp * HPC + h] = L > 0.f ? e / L : 0.f;
+        if (sp == 0) gstat[h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < n_items; e += AT_THREADS) {
+      if (e != tid) load_item(e);
       const int dd = e / (HPC / 8), h8 = e - dd * (HPC / 8);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      constexpr int SB = MAX_SPLITS;   // loads in flight per batch
 #pragma unroll
-      for (int s0 = 0; s0 < MAX_SPLITS; s0 += SB) {
-        uint4 v[SB];
+      for (int sp = 0; sp < MAX_SPLITS; ++sp) {
+        const float4 w0 = *reinterpret_cast<const float4*>(wts + sp * HPC + h8 * 8);
+        const float4 w1 = *reinterpret_cast<const float4*>(wts + sp * HPC + h8 * 8 + 4);
+        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint32_t x[4] = {v[sp].x, v[sp].y, v[sp].z, v[sp].w};
 #pragma unroll
-        for (int s = 0; s < SB; ++s)   // coherent loads: written during this kernel
-          v[s] = s0 + s < (int)n_splits ? ld_cg_v4(part + ((size_t)(s0 + s) * 512 + d_lo + dd) * HPC + h8 * 8)
-                                        : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int s = 0; s < SB; ++s) {
-          const uint32_t w[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-            acc[2 * k] += f.x;
-            acc[2 * k + 1] += f.y;
-          }
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x[k]));
+          acc[2 * k] = fmaf(w[2 * k], f.x, acc[2 * k]);
+          acc[2 * k + 1] = fmaf(w[2 * k + 1], f.y, acc[2 * k + 1]);
         }
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) tr[(h8 * 8 + j) * slice + dd] = acc[j];
     }
+  }
+  {
     __syncthreads();
     const int nc = nd >> 3;
     for (int e = tid; e < HPC * nc; e += AT_THREADS) {

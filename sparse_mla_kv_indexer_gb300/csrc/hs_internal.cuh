@@ -54,6 +54,7 @@ struct Dev {
   int4* miss_list;      // [max_tokens * topk] (layer-group row copies): {req, token, dst_row, 0}
   int32_t* miss_count;  // [max_tokens] misses recorded by the segment starting at each token
   __half* o_part;       // [max_tokens, MAX_SPLITS, 512, 64] fp16 partial attention outputs
+  float2* o_stats;      // [max_tokens, MAX_SPLITS, 64] per split and head: (max in log2 units, sum)
 };
 
 enum Counter { C_RESIDENT = 0, C_HITS = 1, C_MISSES = 2, C_H2D = 3, C_D2H = 4, C_N = 8 };
@@ -242,6 +243,21 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
 
 // ---- distributed shared memory (thread-block clusters) ---------------------------
 // Cluster-wide barrier with release/acquire ordering of shared-memory accesses.
+// Split-phase cluster barrier: every thread of every CTA of the cluster arrives,
+// then waits. A relaxed arrival orders nothing; it only says "this CTA has started",
+// which must hold for every CTA before any of them touches another's shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_v2f(uint32_t addr, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -255,6 +271,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+__device__ __forceinline__ float2 ld_cg_f2(const void* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
 }
 // 16-byte global load that bypasses the non-coherent path (data written by this kernel).
 __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {

@@ -86,6 +86,23 @@ def test_parity_small_configs(name):
         gpu.close()
 
 
+@pytest.mark.parametrize("name,over", [
+    # 16 query tokens x 9 row splits: 64 heads per CTA, merge through L2, odd split count
+    ("small_batch", dict(topk=1152, hot_rows=5 * 1152, pressure=False)),
+    # 1 query token x 9 row splits: 16 heads per CTA, merge through distributed shared memory
+    ("small_single", dict(topk=1152, hot_rows=2 * 1152)),
+])
+def test_parity_odd_split_count(name, over):
+    cfg, wl, plans, oracle, gpu = _setup(name, **over)
+    try:
+        for plan in plans:
+            o = oracle.step(plan)
+            g = gpu.step(plan)
+            check_step(cfg, wl, plan, o, g, gpu, oracle)
+    finally:
+        gpu.close()
+
+
 def test_parity_tiny_all_pages_resident_no_misses():
     cfg, wl, plans, oracle, gpu = _setup("tiny", host_only_frac=0.0)
     try:
