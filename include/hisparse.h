@@ -43,6 +43,11 @@
 extern "C" {
 #endif
 
+/* Longest context a pool accepts (tokens per request). The top-K selection splits a
+ * query token's scores over 16 CTAs and keeps a 2-byte bucket per score of its share
+ * in shared memory, which bounds the share at 81,920 scores. */
+#define HS_MAX_CTX 1310720
+
 typedef struct CUstream_st* hs_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
 typedef enum hs_status {
@@ -71,7 +76,7 @@ typedef struct hs_pool_config {
   int32_t num_pages;          /* pool pages in each layer's KV tensor */
   int32_t num_idx_pages;      /* pages in each indexer layer's key cache */
   int32_t max_requests;       /* request slots */
-  int32_t max_ctx;            /* max positions per request, multiple of 128 */
+  int32_t max_ctx;            /* max positions per request, multiple of 128, <= HS_MAX_CTX */
   int32_t max_q_per_req;      /* query tokens per request per call, 1..4 */
   int32_t hot_rows;           /* hot-buffer capacity per (request, group), multiple of 64 */
   int32_t max_tokens;         /* query tokens per call, 1..1024 */

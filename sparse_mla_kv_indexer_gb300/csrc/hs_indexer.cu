@@ -36,38 +36,51 @@ namespace hs {
 // ----------------------------------------------------------------------------------
 // Scoring kernel
 // ----------------------------------------------------------------------------------
-// Warp roles (320 threads):
-//   warps 0-3  epilogue: TMEM accumulator -> ReLU, head weights, int64 scores
-//   warps 4-7  convert: raw int8 key tile -> fp16 A tile; queries -> fp16 B operand
-//   warp 8     producer: bulk copies of key pages into the stage ring
-//   warp 9     MMA issuer: tcgen05.mma into one of two TMEM accumulators
-constexpr int IX_THREADS = 320;
+// Warp roles (448 threads):
+//   warps 0-3   epilogue: TMEM accumulator -> ReLU, head weights, int64 scores
+//   warps 4-11  convert: raw int8 key tile -> fp16 A tile; queries -> fp16 B operand
+//   warp 12     producer: bulk copies of key pages into the stage ring
+//   warp 13     MMA issuer: tcgen05.mma into one of the TMEM accumulators
+constexpr int IX_THREADS = 448;
+constexpr int IX_CONV = 256;                           // converter threads
+constexpr int IX_PRODUCER_WARP = 12, IX_MMA_WARP = 13;
+constexpr int IX_MAX_A = 4;                            // fp16 A tiles in flight
 constexpr int IX_MAX_STAGES = 12;
 constexpr int IX_TILE = 128;
 constexpr int IX_RAW = IX_TILE * IDX_DIM;              // 16 KB int8 per tile
 constexpr int IX_A_COL = IX_TILE * 128;                // one 64-dim fp16 atom column, 16 KB
 constexpr int IX_A = 2 * IX_A_COL;                     // 32 KB per A tile
 constexpr int IX_SMEM_BUDGET = 227 * 1024;
-constexpr int IX_TMEM_COLS = 512;                      // two accumulators of up to 256 columns
+constexpr int IX_TMEM_COLS = 512;                      // accumulators: 2 x 256 .. 8 x 64 columns
+constexpr int IX_MAX_ACC = 8;
 
 // Shared-memory layout of one launch, sized by the batch geometry so the key
 // ring gets every byte the query operand does not need.
 struct IxLayout {
+  int n_a;        // fp16 A tiles (3 or 4: conversion runs ahead of the MMA)
   int b_col;      // bytes per 64-dim atom column of the query operand (n_max rows x 128 B)
   int off_b, off_raw, off_bar, off_seg, stages, smem;
+  int acc_cols;   // TMEM columns per accumulator (power of two >= n_max rows)
+  int n_acc;      // accumulators in flight between the MMA warp and the epilogue
 };
 
 IxLayout ix_layout(int n_max_rows, int max_tokens) {
   IxLayout L;
   L.b_col = n_max_rows * 128;
-  L.off_b = 2 * IX_A;
-  L.off_raw = L.off_b + 2 * L.b_col;
   const int tail = 512 + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  // as many A tiles as leave at least three key stages, then every remaining byte to the key ring
+  for (L.n_a = IX_MAX_A; L.n_a > 2; --L.n_a)
+    if ((IX_SMEM_BUDGET - L.n_a * IX_A - 2 * L.b_col - tail) / IX_RAW >= 3) break;
+  L.off_b = L.n_a * IX_A;
+  L.off_raw = L.off_b + 2 * L.b_col;
   int stages = (IX_SMEM_BUDGET - L.off_raw - tail) / IX_RAW;
   L.stages = stages > IX_MAX_STAGES ? IX_MAX_STAGES : stages;
   L.off_bar = L.off_raw + L.stages * IX_RAW;
   L.off_seg = L.off_bar + 512;
   L.smem = L.off_seg + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  L.acc_cols = 32;
+  while (L.acc_cols < n_max_rows) L.acc_cols <<= 1;
+  L.n_acc = IX_TMEM_COLS / L.acc_cols < IX_MAX_ACC ? IX_TMEM_COLS / L.acc_cols : IX_MAX_ACC;
   return L;
 }
 
@@ -113,11 +126,11 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   uint64_t* raw_full = bars;                      // [NS]
   uint64_t* raw_empty = bars + IX_MAX_STAGES;     // [NS]
-  uint64_t* a_full = bars + 2 * IX_MAX_STAGES;    // [2]
-  uint64_t* a_empty = a_full + 2;                 // [2]
-  uint64_t* t_full = a_full + 4;                  // [2]
-  uint64_t* t_empty = a_full + 6;                 // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_full + 8);
+  uint64_t* a_full = bars + 2 * IX_MAX_STAGES;    // [n_a]
+  uint64_t* a_empty = a_full + IX_MAX_A;          // [n_a]
+  uint64_t* t_full = a_empty + IX_MAX_A;          // [n_acc]
+  uint64_t* t_empty = t_full + IX_MAX_ACC;        // [n_acc]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + IX_MAX_ACC);
   int32_t* s_nseg = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* s_dead = s_nseg + 1;
   int32_t* s_issued = s_nseg + 2;
@@ -133,7 +146,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
 
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), IX_TMEM_COLS);
   if (tid == 0) {
-    for (int b = 0; b < 2 * IX_MAX_STAGES + 8; ++b) mbar_init(smem_u32(&bars[b]), 1);
+    for (int b = 0; b < 2 * IX_MAX_STAGES + 2 * IX_MAX_A + 2 * IX_MAX_ACC; ++b) mbar_init(smem_u32(&bars[b]), 1);
     fence_mbar_init();
   }
   griddep_wait();
@@ -190,7 +203,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   };
   auto item_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
-  if (warp == 8) {
+  if (warp == IX_PRODUCER_WARP) {
     // ------------------------------ producer ------------------------------
     // Lane l holds the key-page ids of tile (32c + l) of the current chunk c and
     // of the next chunk, so no copy waits on a dependent page-table load.
@@ -240,13 +253,16 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
       }
       if (__shfl_sync(0xffffffffu, dead, 0)) break;
     }
-  } else if (warp == 9) {
+  } else if (warp == IX_MMA_WARP) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
       for (int i = 0; i < n_local; ++i) {
-        const int ab = i & 1;
-        if (!mbar_wait(smem_u32(&a_full[ab]), (i >> 1) & 1, D.status)) { *s_dead = 1; break; }
-        if (i >= 2 && !mbar_wait(smem_u32(&t_empty[ab]), ((i >> 1) - 1) & 1, D.status)) { *s_dead = 1; break; }
+        const int ab = i % L.n_a, tb = i % L.n_acc;
+        if (!mbar_wait(smem_u32(&a_full[ab]), (i / L.n_a) & 1, D.status)) { *s_dead = 1; break; }
+        if (i >= L.n_acc && !mbar_wait(smem_u32(&t_empty[tb]), ((i / L.n_acc) - 1) & 1, D.status)) {
+          *s_dead = 1;
+          break;
+        }
         if (*(volatile int32_t*)s_dead) break;
         tc_fence_after();
         const IxSeg S = segs[seg_of(item_of(i))];
@@ -257,10 +273,10 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
         for (int kk = 0; kk < 8; ++kk) {
           uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * IX_A_COL + (kk & 3) * 32, 16, 1024);
           uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * L.b_col + (kk & 3) * 32, 16, 1024);
-          umma_f16(tmem + ab * 256, ad, bd, idesc, kk > 0);
+          umma_f16(tmem + tb * L.acc_cols, ad, bd, idesc, kk > 0);
         }
         umma_commit(smem_u32(&a_empty[ab]));
-        umma_commit(smem_u32(&t_full[ab]));
+        umma_commit(smem_u32(&t_full[tb]));
       }
     }
   } else if (warp >= 4) {
@@ -276,10 +292,10 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
       bool ok = true;
       if (sg != cur_seg) {
         // every MMA reading the previous queries has completed before they are replaced
-        if (i > 0) ok = mbar_wait(smem_u32(&a_empty[(i - 1) & 1]), ((i - 1) >> 1) & 1, D.status);
+        if (i > 0) ok = mbar_wait(smem_u32(&a_empty[(i - 1) % L.n_a]), ((i - 1) / L.n_a) & 1, D.status);
         uint8_t* B = smem + L.off_b;
         const int N = ((S.ntok * Hi) + 15) & ~15;
-        for (int c = ct; c < N * 8; c += 128) {
+        for (int c = ct; c < N * 8; c += IX_CONV) {
           const int row = c >> 3, ch16 = c & 7;       // 8 chunks of 16 int8 per 128-dim row
           uint4 v = make_uint4(0, 0, 0, 0);
           if (row < S.ntok * Hi) {
@@ -296,18 +312,25 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
         }
         cur_seg = sg;
       }
-      const int rs = i % NS, ab = i & 1;
+      const int rs = i % NS, ab = i % L.n_a;
       if (ok) ok = mbar_wait(smem_u32(&raw_full[rs]), (i / NS) & 1, D.status);
-      if (ok && i >= 2) ok = mbar_wait(smem_u32(&a_empty[ab]), ((i >> 1) - 1) & 1, D.status);
+      if (ok && i >= L.n_a) ok = mbar_wait(smem_u32(&a_empty[ab]), ((i / L.n_a) - 1) & 1, D.status);
       if (!ok) *s_dead = 1;
       const uint8_t* raw = smem + L.off_raw + rs * IX_RAW;
       uint8_t* A = smem + ab * IX_A;
-      for (int c = ct; c < IX_TILE * 8; c += 128) {
-        const int row = c >> 3, ch16 = c & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (key0 + row < S.maxlim) v = *reinterpret_cast<const uint4*>(raw + row * IDX_DIM + ch16 * 16);
+      constexpr int CPT = IX_TILE * 8 / IX_CONV;   // 16-byte chunks per converter thread
+      uint4 v[CPT];
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {   // all loads first
+        const int c = ct + k * IX_CONV, row = c >> 3, ch16 = c & 7;
+        v[k] = key0 + row < S.maxlim ? *reinterpret_cast<const uint4*>(raw + row * IDX_DIM + ch16 * 16)
+                                     : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        const int c = ct + k * IX_CONV, row = c >> 3, ch16 = c & 7;
         uint4 c0, c1;
-        i8x16_to_f16(v, c0, c1);
+        i8x16_to_f16(v[k], c0, c1);
         const int dim0 = ch16 * 16;
         uint8_t* base = A + (dim0 >> 6) * IX_A_COL;
         const int chunk = (dim0 & 63) >> 3;
@@ -315,7 +338,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
         *reinterpret_cast<uint4*>(base + sw128_chunk(row, chunk + 1)) = c1;
       }
       fence_proxy_async();
-      named_sync(1, 128);
+      named_sync(1, IX_CONV);
       if (ct == 0) {
         *s_consumed = i + 1;
         mbar_arrive(smem_u32(&raw_empty[rs]));
@@ -347,32 +370,50 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
         named_sync(2, 128);
         cur_seg = sg;
       }
-      const int ab = i & 1;
-      if (!mbar_wait(smem_u32(&t_full[ab]), (i >> 1) & 1, D.status)) { *s_dead = 1; break; }
+      const int tb = i % L.n_acc;
+      if (!mbar_wait(smem_u32(&t_full[tb]), (i / L.n_acc) & 1, D.status)) { *s_dead = 1; break; }
       tc_fence_after();
+      // Exact integer epilogue without float->int conversions: every dot product
+      // is an integer |d| <= 2^21 held exactly in fp32, so max(d, 0) + 2^23 carries
+      // it in the low mantissa bits. With w <= 127, each w * relu(d) < 2^28 and 16
+      // of them sum below 2^32: 16 heads accumulate in uint32, the groups in 64 bits.
       for (int j = 0; j < S.ntok; ++j) {
         const int lim = s_lim[S.first + j];
-        long long acc = 0;
-        for (int h0 = 0; h0 < Hi; h0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(lane_base + (uint32_t)(ab * 256 + j * Hi + h0), r);
-          tmem_wait_ld();
+        const uint32_t col0 = lane_base + (uint32_t)(tb * L.acc_cols + j * Hi);
+        uint32_t r[64];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int v = max(__float2int_rn(__uint_as_float(r[k])), 0);
-            acc += (long long)v * s_w[j * 64 + h0 + k];
+        for (int q = 0; q < 4; ++q)
+          if (q * 16 < Hi) tmem_ld16(col0 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(r + q * 16));
+        tmem_wait_ld();
+        unsigned long long acc = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q * 16 < Hi) {
+            uint32_t s32 = 0;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int4 w4 = *reinterpret_cast<const int4*>(s_w + j * 64 + q * 16 + k4 * 4);
+              const int w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float d = fmaxf(__uint_as_float(r[q * 16 + k4 * 4 + k]), 0.f);
+                const uint32_t u = __float_as_uint(d + 8388608.f) - 0x4B000000u;
+                s32 += u * (uint32_t)w[k];
+              }
+            }
+            acc += s32;
           }
         }
-        if (key < lim) scores[(size_t)(S.first + j) * ld + key] = acc;
+        if (key < lim) scores[(size_t)(S.first + j) * ld + key] = (long long)acc;
       }
       tc_fence_before();
       named_sync(2, 128);
-      if (tid == 0) mbar_arrive(smem_u32(&t_empty[ab]));
+      if (tid == 0) mbar_arrive(smem_u32(&t_empty[tb]));
       if (*(volatile int32_t*)s_dead) break;
     }
   }
   __syncthreads();
-  if (*s_dead && tid == 8 * 32) {
+  if (*s_dead && tid == IX_PRODUCER_WARP * 32) {
     // drain bulk copies still in flight before the CTA's shared memory goes away
     for (int k = *s_consumed; k < *s_issued; ++k)
       mbar_wait(smem_u32(&raw_full[k % NS]), (k / NS) & 1, D.status);
@@ -395,7 +436,17 @@ constexpr int SEL_BINS = 4096;
 constexpr int SEL_CACHE = 12288;                       // keys cached in shared memory per CTA
 constexpr int SEL_CAND = 2048;                         // candidates per CTA on the fast path
 constexpr int SEL_LEAD = 4096;                         // candidates the cluster leader sorts
-constexpr int SEL_SMEM = SEL_CACHE * 8 + SEL_CACHE * 2 + SEL_LEAD * 8 + SEL_CAND * 8 + 1024;
+constexpr int SEL_PIECE = 2048;                       // keys per bulk copy of the streaming pass
+constexpr int SEL_RING = 3;                            // pieces in flight
+constexpr int SEL_STREAM_MAX = 81920;                  // keys per CTA whose buckets fit in shared memory
+static_assert(16 * SEL_STREAM_MAX == HS_MAX_CTX, "the longest context fits the streaming pass");
+// two layouts of the dynamic shared memory, chosen per launch by the chunk size:
+//  cached    [keys SEL_CACHE x 8 B][lead][cand][buckets SEL_CACHE x 2 B]
+//  streaming [buckets SEL_STREAM_MAX x 2 B][ring SEL_RING pieces; after pass 1: lead, cand]
+constexpr int SEL_SMEM_CACHED = SEL_CACHE * 8 + SEL_CACHE * 2 + SEL_LEAD * 8 + SEL_CAND * 8;
+constexpr int SEL_SMEM_STREAM = SEL_STREAM_MAX * 2 + SEL_RING * SEL_PIECE * 8;
+constexpr int SEL_SMEM = (SEL_SMEM_CACHED > SEL_SMEM_STREAM ? SEL_SMEM_CACHED : SEL_SMEM_STREAM) + 16;
+static_assert(SEL_LEAD * 8 + SEL_CAND * 8 <= SEL_RING * SEL_PIECE * 8, "lead and cand fit in the ring");
 constexpr unsigned long long IDX_MASK = (1ull << 21) - 1;
 
 // monotone level-0 bucket of a key: exact below 64, then 64 buckets per octave
@@ -470,13 +521,8 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   __shared__ int s_cnt[CL];
   __shared__ long long s_above;
   __shared__ unsigned long long s_tau;
-  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_bar[SEL_RING];
   extern __shared__ __align__(16) uint8_t sel_dyn[];
-  unsigned long long* cache = reinterpret_cast<unsigned long long*>(sel_dyn);            // [SEL_CACHE]
-  unsigned long long* lead = cache + SEL_CACHE;                                           // [SEL_LEAD]
-  unsigned long long* cand = lead + SEL_LEAD;                                             // [SEL_CAND]
-  uint16_t* bk = reinterpret_cast<uint16_t*>(cand + SEL_CAND);                            // [SEL_CACHE] buckets
-  int32_t* elist = reinterpret_cast<int32_t*>(lead);                                      // [K] after tau
 
   griddep_wait();
   griddep_launch();
@@ -492,7 +538,18 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   const int per = ((n + CL - 1) / CL + 1) & ~1;   // even, so every chunk starts 16-byte aligned
   const int lo = min(n, crank * per), hi = min(n, lo + per);
   const int cnt_local = max(0, hi - lo);
+  // cached: the chunk's keys stay in shared memory; streaming (longer chunks, up to
+  // SEL_STREAM_MAX since max_ctx <= HS_MAX_CTX): only their buckets do, and keys of
+  // the threshold bucket are re-read from L2
   const bool cached = per <= SEL_CACHE;
+  unsigned long long* cache = reinterpret_cast<unsigned long long*>(sel_dyn);             // cached: [SEL_CACHE]
+  unsigned long long* lead = cached ? cache + SEL_CACHE                                    // [SEL_LEAD]
+                                    : reinterpret_cast<unsigned long long*>(sel_dyn + SEL_STREAM_MAX * 2);
+  unsigned long long* cand = lead + SEL_LEAD;                                              // [SEL_CAND]
+  unsigned long long* ring = lead;                                                         // streaming pass 1
+  uint16_t* bk = cached ? reinterpret_cast<uint16_t*>(cand + SEL_CAND)                    // [chunk] buckets
+                        : reinterpret_cast<uint16_t*>(sel_dyn);
+  int32_t* elist = reinterpret_cast<int32_t*>(lead);                                       // [K] after tau
   auto key_at = [&](int i) -> unsigned long long {
     if (cached) return cache[i];
     long long v = s[lo + i];
@@ -503,8 +560,8 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = 0;
   if (tid == 0) {
     s_ncand = 0; s_over = 0; s_bin = 0; s_above = 0;
-    if (cached) {
-      mbar_init(smem_u32(&s_bar), 1);
+    {
+      for (int r = 0; r < SEL_RING; ++r) mbar_init(smem_u32(&s_bar[r]), 1);
       fence_mbar_init();
     }
   }
@@ -513,13 +570,13 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
     // the whole chunk arrives by bulk copy (TMA unit) in one round trip
     const int even = cnt_local & ~1;
     if (tid == 0) {
-      const uint32_t bar = smem_u32(&s_bar);
+      const uint32_t bar = smem_u32(&s_bar[0]);
       mbar_expect_tx(bar, (uint32_t)even * 8u);
       for (int off = 0; off < even; off += 4096)
         bulk_g2s(smem_u32(cache + off), s + lo + off, (uint32_t)min(4096, even - off) * 8u, bar);
     }
     if (tid == 0 && (cnt_local & 1)) cache[cnt_local - 1] = (unsigned long long)s[lo + cnt_local - 1];
-    if (!mbar_wait(smem_u32(&s_bar), 0, D.status)) { /* recorded; the data below is then unreliable */ }
+    if (!mbar_wait(smem_u32(&s_bar[0]), 0, D.status)) { /* recorded; the data below is then unreliable */ }
     __syncthreads();
 #pragma unroll 4
     for (int i = tid; i < cnt_local; i += blockDim.x) {
@@ -532,11 +589,45 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
       hist_add(hist, b);
     }
   } else {
-    for (int i = tid; i < cnt_local; i += blockDim.x) {
-      long long v = s[lo + i];
-      if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
-      hist_add(hist, bucket1(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + i))));
+    // pieces of SEL_PIECE scores stream through a ring of bulk copies; each key's
+    // bucket is kept, the key itself is not
+    const int even = cnt_local & ~1;
+    const int n_pieces = (even + SEL_PIECE - 1) / SEL_PIECE;
+    auto issue = [&](int pc) {
+      const int off = pc * SEL_PIECE, cnt = min(SEL_PIECE, even - off);
+      const uint32_t bar = smem_u32(&s_bar[pc % SEL_RING]);
+      mbar_expect_tx(bar, (uint32_t)cnt * 8u);
+      bulk_g2s(smem_u32(ring + (pc % SEL_RING) * SEL_PIECE), s + lo + off, (uint32_t)cnt * 8u, bar);
+    };
+    if (tid == 0)
+      for (int pc = 0; pc < SEL_RING && pc < n_pieces; ++pc) issue(pc);
+    for (int pc = 0; pc < n_pieces; ++pc) {
+      const bool ok = mbar_wait(smem_u32(&s_bar[pc % SEL_RING]), (pc / SEL_RING) & 1, D.status);
+      if (__syncthreads_or(!ok)) break;   // a timeout (recorded) ends the pass for every thread
+      const unsigned long long* piece = ring + (pc % SEL_RING) * SEL_PIECE;
+      const int off = pc * SEL_PIECE, cnt = min(SEL_PIECE, even - off);
+#pragma unroll 4
+      for (int i = tid; i < cnt; i += blockDim.x) {
+        long long v = (long long)piece[i];
+        if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
+        const int b = bucket1(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + off + i)));
+        bk[off + i] = (uint16_t)b;
+        hist_add(hist, b);
+      }
+      __syncthreads();   // the stage is read; it may be refilled
+      if (tid == 0 && pc + SEL_RING < n_pieces) {
+        fence_proxy_async();
+        issue(pc + SEL_RING);
+      }
     }
+    if (tid == 0 && (cnt_local & 1)) {
+      long long v = s[lo + cnt_local - 1];
+      if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
+      const int b = bucket1(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + cnt_local - 1)));
+      bk[cnt_local - 1] = (uint16_t)b;
+      hist_add(hist, b);
+    }
+    __syncthreads();
   }
   int need = K;
   auto cluster_find = [&](void) {
@@ -582,7 +673,7 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   // ---- fast path: collect the keys of bucket B0, the leader sorts them ----
 #pragma unroll 4
   for (int i = tid; i < cnt_local; i += blockDim.x) {
-    if (cached ? bk[i] == B0 : bucket1(key_at(i)) == B0) {
+    if (bk[i] == B0) {
       const unsigned long long k = key_at(i);
       int at = atomicAdd(&s_ncand, 1);
       if (at < SEL_CAND) cand[at] = k; else s_over = 1;
@@ -657,9 +748,14 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   constexpr int NW = SEL_THREADS / 32;
   const int wper = (cnt_local + NW - 1) / NW;
   const int wlo = min(cnt_local, wid * wper), whi = min(cnt_local, wlo + wper);
+  // a key is selected when its bucket is above B0, or it is in B0 and not below tau
+  auto selected = [&](int i) -> bool {
+    const int b = bk[i];
+    return b > B0 || (b == B0 && key_at(i) >= tau);
+  };
   int wcount = 0;
 #pragma unroll 4
-  for (int i = wlo + lane; i < whi; i += 32) wcount += key_at(i) >= tau;
+  for (int i = wlo + lane; i < whi; i += 32) wcount += selected(i);
   wcount = __reduce_add_sync(0xffffffffu, wcount);
   if (lane == 0) warp_tot[wid] = wcount;
   __syncthreads();
@@ -669,7 +765,7 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   for (int w = 0; w < NW; ++w) sel_run += warp_tot[w];
   for (int i0 = wlo; i0 < whi; i0 += 32) {
     const int i = i0 + lane;
-    const bool sel = i < whi && key_at(i) >= tau;
+    const bool sel = i < whi && selected(i);
     const unsigned m = __ballot_sync(0xffffffffu, sel);
     if (sel) {
       const int pos = wbase + __popc(m & ((1u << lane) - 1));

@@ -157,7 +157,7 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   if (c.num_pages < 1 || c.num_idx_pages < 1 || c.max_requests < 1 || c.max_ctx < 128 || c.max_ctx % 128)
     return HS_ERR_INVALID;
   if ((long long)c.num_pages * PAGE >= (1ll << 31)) return HS_ERR_INVALID;
-  if (c.max_ctx >= (1 << 21)) return HS_ERR_INVALID;   // token ids fit the 21-bit tie-break field
+  if (c.max_ctx > HS_MAX_CTX) return HS_ERR_INVALID;   // also keeps token ids within the 21-bit tie-break field
   if (c.max_q_per_req < 1 || c.max_q_per_req > 4 || c.max_q_per_req * c.topk > 8192) return HS_ERR_INVALID;
   if (c.max_q_per_req * c.n_idx_heads > 256) return HS_ERR_INVALID;
   if (c.hot_rows < PAGE || c.hot_rows % PAGE || c.hot_rows > 16384) return HS_ERR_INVALID;

@@ -19,6 +19,7 @@ STATUS = {
     9: "HS_ERR_SCRATCH_LIMIT",
 }
 PLAN_PAD, PLAN_RESIDENT, PLAN_HIT, PLAN_MISS = 0, 1, 2, 3
+MAX_CTX = 1310720            # HS_MAX_CTX: longest context a pool accepts
 
 
 class HisparseError(RuntimeError):

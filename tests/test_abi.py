@@ -73,3 +73,13 @@ def test_bad_geometry_is_invalid(lib):
     cfg = PoolConfig(**good)
     misaligned = (ctypes.c_void_p * 8)(*([24] * 8))
     assert lib.hs_pool_init(ctypes.byref(cfg), misaligned, ptrs, ctypes.c_void_p(16), ctypes.byref(out)) == 1
+
+
+def test_binding_constants_match_the_header():
+    from sparse_mla_kv_indexer_gb300 import hisparse as H
+    text = open(HEADER).read()
+    defines = dict(re.findall(r"#define\s+(HS_[A-Z_]+)\s+\(?([0-9a-fx]+(?:ll)?(?:\s*<<\s*\d+)?)\)?", text))
+    assert int(defines["HS_MAX_CTX"]) == H.MAX_CTX
+    assert H.MAX_CTX % 128 == 0 and H.MAX_CTX < (1 << 21)   # token ids fit the 21-bit tie-break field
+    for code, name in H.STATUS.items():
+        assert re.search(rf"\b{name}\s*=\s*{code}\b", text), name
