@@ -53,7 +53,17 @@ struct AtPlan {
   static constexpr int Q_COL = HPC * 128;                 // one 64-dim atom column of Q [HPC][576]
   static constexpr int P_G = 2 * HPC * 128;               // one P_g [HPC heads][128 rows] bf16
   static constexpr int OFF_MISC = AT_OFF_Q + 9 * Q_COL;
-  static constexpr int SMEM = OFF_MISC + AT_MISC + 1024;
+  // Up to 32 heads the splits merge in shared memory: each CTA receives, by
+  // asynchronous remote stores, every split's per-head (max, sum) and the fp16
+  // partials of its own slice of the output dims. At 64 heads that does not fit;
+  // the merge goes through an L2-resident buffer instead.
+  static constexpr bool DSM = HPC <= 32;
+  static constexpr int RECV_DIMS = HPC == 16 ? 600 : 512;         // splits x slice dims it can receive
+  static constexpr int RECV = DSM ? RECV_DIMS * HPC * 2 : 0;      // [split][slice dim][HPC] fp16
+  static constexpr int STATS = DSM ? MAX_SPLITS * HPC * 8 : 0;    // [split][HPC] (max, sum)
+  static constexpr int OFF_RECV = OFF_MISC + AT_MISC;
+  static constexpr int OFF_STATS = OFF_RECV + RECV;
+  static constexpr int SMEM = OFF_STATS + STATS + 1024;
   static constexpr int HW = HPC / 4;                      // heads per warp in the softmax
   static_assert(4 * P_G <= 9 * Q_COL, "P_0..P_3 fit in the query region");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -129,8 +139,10 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   float* lfin = mfin + HPC;                                                  // [HPC] this split's sum
   float* wmine = lfin + HPC;                                                 // [HPC] weight of this split
   float* gstat = wmine + HPC;                                                // [HPC] lse
-  uint64_t* bar = reinterpret_cast<uint64_t*>(gstat + HPC);                  // [2] QK, PV completion
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gstat + HPC);                  // [4] QK, PV, stats in, partials in
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 4);
+  __half* recv = reinterpret_cast<__half*>(smem + PL::OFF_RECV);
+  float* rstats = reinterpret_cast<float*>(smem + PL::OFF_STATS);
 
   const uint32_t split = cluster_rank();
   const uint32_t n_splits = cluster_size();
@@ -142,11 +154,23 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   const long long max_row = (long long)D.num_pages * PAGE;
 
   if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
+  // this CTA's slice of the 512 output dims in the split merge
+  const int slice = ((512 + (int)n_splits - 1) / (int)n_splits + 7) & ~7;
+  const int d_lo = min(512, (int)split * slice), d_hi = min(512, d_lo + slice);
+  const int nd = d_hi - d_lo;
   if (tid == 0) {
     mbar_init(smem_u32(bar), 5);       // one arrival per QK accumulator
     mbar_init(smem_u32(bar + 1), 4);   // one arrival per PV group
+    if constexpr (PL::DSM) {
+      mbar_init(smem_u32(bar + 2), 1);
+      mbar_init(smem_u32(bar + 3), 1);
+      // the bytes every split will store here: (max, sum) of all heads, partials of the slice
+      mbar_expect_tx(smem_u32(bar + 2), n_splits * HPC * 8);
+      mbar_expect_tx(smem_u32(bar + 3), n_splits * nd * HPC * 2);
+    }
     fence_mbar_init();
   }
+  if constexpr (PL::DSM) cluster_arrive_relaxed();   // this CTA has started; its barriers are initialised
   griddep_wait();
   griddep_launch();
   if (tid < ATTN_ROWS) {
@@ -333,98 +357,72 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     }
     umma_commit(smem_u32(bar + 1));
   }
-  // while PV runs: this split's per-head (max, sum) to the token's merge record
-  float2* stats = D.o_stats + (size_t)tok * MAX_SPLITS * 64;          // [split][64 heads]
-  if (tid >= 128 && tid < 128 + HPC) {
-    const int h = tid - 128;
-    const float l = red[h] + red[HPC + h] + red[2 * HPC + h] + red[3 * HPC + h];
-    lfin[h] = l;
-    stats[(size_t)split * 64 + hgrp * HPC + h] = make_float2(mfin[h], l);
-  }
-  ok &= mbar_wait(smem_u32(bar + 1), 0, D.status);
-  tc_fence_after();
-  __syncthreads();   // lfin
-
-  // ---- the split's partial O, normalised by its own sum, in fp16 to the merge buffer ----
-  // layout per (token, head group): [split][dim][HPC]; warp (row quadrant, group g)
-  __half* part = D.o_part + (size_t)tok * MAX_SPLITS * 512 * 64 + (size_t)hgrp * MAX_SPLITS * 512 * HPC;
-  {
-    const int g = sub;
-    const int dim = g * 128 + quad * 32 + lane;
-    constexpr int CW = HPC < 32 ? HPC : 32;   // columns per TMEM read
-    uint4* dst = reinterpret_cast<uint4*>(part + ((size_t)split * 512 + dim) * HPC);
-#pragma unroll
-    for (int h0 = 0; h0 < HPC; h0 += CW) {
-      uint32_t r[CW];
-      tmem_ld_cols<CW>(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 64 + h0), r);
+  if constexpr (PL::DSM) {
+    // while PV runs: this split's per-head (max, sum) into every CTA of the cluster
+    cluster_wait_acquire();   // every CTA has started and initialised its barriers
+    if (tid >= 128 && tid < 128 + HPC) {
+      const int h = tid - 128;
+      const float l = red[h] + red[HPC + h] + red[2 * HPC + h] + red[3 * HPC + h];
+      lfin[h] = l;
+      const uint32_t a = smem_u32(rstats + ((int)split * HPC + h) * 2), rb = smem_u32(bar + 2);
+      for (uint32_t d = 0; d < n_splits; ++d) st_async_v2f(mapa(a, d), mfin[h], l, mapa(rb, d));
+    }
+    ok &= mbar_wait(smem_u32(bar + 1), 0, D.status);
+    tc_fence_after();
+    __syncthreads();   // lfin
+    // ---- the split's partial O, normalised by its own sum, in fp16 straight into the
+    //      shared memory of the CTA that owns the dims: warp (row quadrant, group g) ----
+    {
+      const int g = sub;
+      const int dim = g * 128 + quad * 32 + lane;
+      const int owner = dim / slice;
+      const uint32_t dst = mapa(smem_u32(recv + ((size_t)split * slice + (dim - owner * slice)) * HPC), owner);
+      const uint32_t rb = mapa(smem_u32(bar + 3), owner);
+      uint32_t r[HPC];
+      tmem_ld_cols<HPC>(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 64), r);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < CW / 8; ++c) {
+      for (int c = 0; c < HPC / 8; ++c) {
         uint32_t hv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int h = h0 + c * 8 + 2 * i;
+          const int h = c * 8 + 2 * i;
           const float i0 = lfin[h] > 0.f ? 1.f / lfin[h] : 0.f, i1 = lfin[h + 1] > 0.f ? 1.f / lfin[h + 1] : 0.f;
-          __half2 h2 = __floats2half2_rn(__uint_as_float(r[h - h0]) * i0, __uint_as_float(r[h - h0 + 1]) * i1);
+          __half2 h2 = __floats2half2_rn(__uint_as_float(r[h]) * i0, __uint_as_float(r[h + 1]) * i1);
           hv[i] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        dst[(h0 >> 3) + c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        st_async_v4(dst + c * 16, make_uint4(hv[0], hv[1], hv[2], hv[3]), rb);
       }
     }
-  }
-  // one cluster barrier: every split's (max, sum) and partial are written (cluster scope)
-  tc_fence_before();
-  cluster_arrive_release();
-  cluster_wait_acquire();
-
-  // ---- this CTA's slice of the 512 dims: the partials are loaded first, so their
-  //      round trip to L2 overlaps the one for the (max, sum) of the splits ----
-  const int slice = ((512 + (int)n_splits - 1) / (int)n_splits + 7) & ~7;
-  const int d_lo = min(512, (int)split * slice), d_hi = min(512, d_lo + slice);
-  const int nd = d_hi - d_lo;
-  float* wts = reinterpret_cast<float*>(KV);            // [MAX_SPLITS][HPC]; the KV tile is no longer read
-  float* tr = wts + MAX_SPLITS * HPC;                    // [HPC][slice] fp32 transpose
-  {
-    // items (dim, 8 heads); a thread's first item is loaded before the weights are known
-    const int n_items = nd * (HPC / 8);
-    uint4 v[MAX_SPLITS];
-    auto load_item = [&](int e) {
-      const int dd = e / (HPC / 8), h8 = e - dd * (HPC / 8);
+    // ---- weights of the splits per head (16-lane group per head), from this CTA's copy ----
+    float* wts = reinterpret_cast<float*>(KV);            // [MAX_SPLITS][HPC]; the KV tile is no longer read
+    float* tr = wts + MAX_SPLITS * HPC;                    // [HPC][slice] fp32 transpose
+    ok &= mbar_wait(smem_u32(bar + 2), 0, D.status);
+    if (tid < MAX_SPLITS * HPC) {                          // whole warps (16 x HPC is a multiple of 32)
+      const int h = tid >> 4, sp = tid & 15;
+      const float2 ml = sp < (int)n_splits ? *reinterpret_cast<const float2*>(rstats + (sp * HPC + h) * 2)
+                                           : make_float2(-INFINITY, 0.f);
+      float M = ml.x;
 #pragma unroll
-      for (int sp = 0; sp < MAX_SPLITS; ++sp)   // coherent loads: written during this kernel
-        v[sp] = sp < (int)n_splits ? ld_cg_v4(part + ((size_t)sp * 512 + d_lo + dd) * HPC + h8 * 8)
-                                   : make_uint4(0, 0, 0, 0);
-    };
-    if (tid < n_items) load_item(tid);
-    // weights of the splits per head: a 16-lane group per head, one lane per split
-    for (int t0 = 0; t0 < MAX_SPLITS * HPC; t0 += AT_THREADS) {
-      const int t = t0 + tid;
-      if (t0 + (tid & ~31) < MAX_SPLITS * HPC) {           // whole warps only: shuffles below
-        const int h = t >> 4, sp = t & 15;
-        const float2 ml = sp < (int)n_splits ? ld_cg_f2(stats + (size_t)sp * 64 + hgrp * HPC + h)
-                                             : make_float2(-INFINITY, 0.f);
-        float M = ml.x;
+      for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float e = ml.x == -INFINITY ? 0.f : ml.y * exp2f(ml.x - M);
+      float L = e;
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float e = ml.x == -INFINITY ? 0.f : ml.y * exp2f(ml.x - M);
-        float L = e;
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        wts[sp * HPC + h] = L > 0.f ? e / L : 0.f;
-        if (sp == 0) gstat[h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-      }
+      for (int o = 8; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      wts[sp * HPC + h] = L > 0.f ? e / L : 0.f;
+      if (sp == 0) gstat[h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();
-    for (int e = tid; e < n_items; e += AT_THREADS) {
-      if (e != tid) load_item(e);
+    ok &= mbar_wait(smem_u32(bar + 3), 0, D.status);   // every split's partials of this slice
+    for (int e = tid; e < nd * (HPC / 8); e += AT_THREADS) {
       const int dd = e / (HPC / 8), h8 = e - dd * (HPC / 8);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int sp = 0; sp < MAX_SPLITS; ++sp) {
+      for (int sp = 0; sp < (int)n_splits; ++sp) {
+        const uint4 v = *reinterpret_cast<const uint4*>(recv + ((size_t)sp * slice + dd) * HPC + h8 * 8);
         const float4 w0 = *reinterpret_cast<const float4*>(wts + sp * HPC + h8 * 8);
         const float4 w1 = *reinterpret_cast<const float4*>(wts + sp * HPC + h8 * 8 + 4);
         const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const uint32_t x[4] = {v[sp].x, v[sp].y, v[sp].z, v[sp].w};
+        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x[k]));
@@ -435,8 +433,6 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
 #pragma unroll
       for (int j = 0; j < 8; ++j) tr[(h8 * 8 + j) * slice + dd] = acc[j];
     }
-  }
-  {
     __syncthreads();
     const int nc = nd >> 3;
     for (int e = tid; e < HPC * nc; e += AT_THREADS) {
@@ -447,6 +443,119 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
                      pack_bf16x2(src[6], src[7]));
     }
     if (split == 0 && lse_out && tid < HPC) lse_out[(size_t)tok * H + (size_t)hgrp * HPC + tid] = gstat[tid];
+  } else {
+    // while PV runs: this split's per-head (max, sum) to the token's merge record
+    float2* stats = D.o_stats + (size_t)tok * MAX_SPLITS * 64;          // [split][64 heads]
+    if (tid >= 128 && tid < 128 + HPC) {
+      const int h = tid - 128;
+      const float l = red[h] + red[HPC + h] + red[2 * HPC + h] + red[3 * HPC + h];
+      lfin[h] = l;
+      stats[(size_t)split * 64 + hgrp * HPC + h] = make_float2(mfin[h], l);
+    }
+    ok &= mbar_wait(smem_u32(bar + 1), 0, D.status);
+    tc_fence_after();
+    __syncthreads();   // lfin
+
+    // ---- the split's partial O, normalised by its own sum, in fp16 to the merge buffer ----
+    // layout per (token, head group): [split][dim][HPC]; warp (row quadrant, group g)
+    __half* part = D.o_part + (size_t)tok * MAX_SPLITS * 512 * 64 + (size_t)hgrp * MAX_SPLITS * 512 * HPC;
+    {
+      const int g = sub;
+      const int dim = g * 128 + quad * 32 + lane;
+      constexpr int CW = HPC < 32 ? HPC : 32;   // columns per TMEM read
+      uint4* dst = reinterpret_cast<uint4*>(part + ((size_t)split * 512 + dim) * HPC);
+#pragma unroll
+      for (int h0 = 0; h0 < HPC; h0 += CW) {
+        uint32_t r[CW];
+        tmem_ld_cols<CW>(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 64 + h0), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < CW / 8; ++c) {
+          uint32_t hv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int h = h0 + c * 8 + 2 * i;
+            const float i0 = lfin[h] > 0.f ? 1.f / lfin[h] : 0.f, i1 = lfin[h + 1] > 0.f ? 1.f / lfin[h + 1] : 0.f;
+            __half2 h2 = __floats2half2_rn(__uint_as_float(r[h - h0]) * i0, __uint_as_float(r[h - h0 + 1]) * i1);
+            hv[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          dst[(h0 >> 3) + c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
+      }
+    }
+    // one cluster barrier: every split's (max, sum) and partial are written (cluster scope)
+    tc_fence_before();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+
+    // ---- this CTA's slice of the 512 dims: the partials are loaded first, so their
+    //      round trip to L2 overlaps the one for the (max, sum) of the splits ----
+    float* wts = reinterpret_cast<float*>(KV);            // [MAX_SPLITS][HPC]; the KV tile is no longer read
+    float* tr = wts + MAX_SPLITS * HPC;                    // [HPC][slice] fp32 transpose
+    {
+      // items (dim, 8 heads); a thread's first item is loaded before the weights are known
+      const int n_items = nd * (HPC / 8);
+      uint4 v[MAX_SPLITS];
+      auto load_item = [&](int e) {
+        const int dd = e / (HPC / 8), h8 = e - dd * (HPC / 8);
+#pragma unroll
+        for (int sp = 0; sp < MAX_SPLITS; ++sp)   // coherent loads: written during this kernel
+          v[sp] = sp < (int)n_splits ? ld_cg_v4(part + ((size_t)sp * 512 + d_lo + dd) * HPC + h8 * 8)
+                                     : make_uint4(0, 0, 0, 0);
+      };
+      if (tid < n_items) load_item(tid);
+      // weights of the splits per head: a 16-lane group per head, one lane per split
+      for (int t0 = 0; t0 < MAX_SPLITS * HPC; t0 += AT_THREADS) {
+        const int t = t0 + tid;
+        if (t0 + (tid & ~31) < MAX_SPLITS * HPC) {           // whole warps only: shuffles below
+          const int h = t >> 4, sp = t & 15;
+          const float2 ml = sp < (int)n_splits ? ld_cg_f2(stats + (size_t)sp * 64 + hgrp * HPC + h)
+                                               : make_float2(-INFINITY, 0.f);
+          float M = ml.x;
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+          const float e = ml.x == -INFINITY ? 0.f : ml.y * exp2f(ml.x - M);
+          float L = e;
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+          wts[sp * HPC + h] = L > 0.f ? e / L : 0.f;
+          if (sp == 0) gstat[h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        }
+      }
+      __syncthreads();
+      for (int e = tid; e < n_items; e += AT_THREADS) {
+        if (e != tid) load_item(e);
+        const int dd = e / (HPC / 8), h8 = e - dd * (HPC / 8);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int sp = 0; sp < MAX_SPLITS; ++sp) {
+          const float4 w0 = *reinterpret_cast<const float4*>(wts + sp * HPC + h8 * 8);
+          const float4 w1 = *reinterpret_cast<const float4*>(wts + sp * HPC + h8 * 8 + 4);
+          const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const uint32_t x[4] = {v[sp].x, v[sp].y, v[sp].z, v[sp].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x[k]));
+            acc[2 * k] = fmaf(w[2 * k], f.x, acc[2 * k]);
+            acc[2 * k + 1] = fmaf(w[2 * k + 1], f.y, acc[2 * k + 1]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tr[(h8 * 8 + j) * slice + dd] = acc[j];
+      }
+    }
+    {
+      __syncthreads();
+      const int nc = nd >> 3;
+      for (int e = tid; e < HPC * nc; e += AT_THREADS) {
+        const int h = e / nc, c = e - h * nc;
+        const float* src = tr + h * slice + c * 8;
+        *reinterpret_cast<uint4*>(out + ((size_t)tok * H + (size_t)hgrp * HPC + h) * 512 + d_lo + c * 8) =
+            make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]), pack_bf16x2(src[4], src[5]),
+                       pack_bf16x2(src[6], src[7]));
+      }
+      if (split == 0 && lse_out && tid < HPC) lse_out[(size_t)tok * H + (size_t)hgrp * HPC + tid] = gstat[tid];
+    }
   }
   (void)ok;
   __syncthreads();
@@ -477,6 +586,8 @@ hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, co
   // fewer heads per CTA while the head groups still fit on the SMs side by side
   int hpc = H < 64 ? H : 64;
   while (hpc > 16 && (long long)n * n_splits * (H / (hpc / 2)) <= num_sms()) hpc /= 2;
+  const int slice = ((512 + n_splits - 1) / n_splits + 7) & ~7;
+  if (hpc == 32 && n_splits * slice > AtPlan<32>::RECV_DIMS) hpc = 16;   // receive buffer bound
   const float sl = sm_scale * LOG2E;
   if (hpc == 16) return launch_attention_hpc<16>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
   if (hpc == 32) return launch_attention_hpc<32>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
