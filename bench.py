@@ -436,7 +436,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": 1000.0 * t_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8/fp8-e4m3 x fp16 tensor cores, fp32 accumulate",
+        "dtype": "int8->int64 (indexer, exact), fp8-e4m3/bf16->fp32 (attention)",
         "data": "synthetic",
         "config": {"workload": args.workload, "requests_per_gpu": cfg.n_requests,
                    "context": list(cfg.ctx_len)[:4], "heads": cfg.n_heads, "topk": cfg.topk,

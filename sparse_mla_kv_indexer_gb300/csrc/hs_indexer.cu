@@ -67,7 +67,7 @@ struct IxLayout {
 IxLayout ix_layout(int n_max_rows, int max_tokens) {
   IxLayout L;
   L.b_col = n_max_rows * 128;
-  const int tail = 512 + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  const int tail = 512 + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 64 + 1024;
   // as many A tiles as leave at least three key stages, then every remaining byte to the key ring
   for (L.n_a = IX_MAX_A; L.n_a > 2; --L.n_a)
     if ((IX_SMEM_BUDGET - L.n_a * IX_A - 2 * L.b_col - tail) / IX_RAW >= 3) break;
@@ -77,7 +77,7 @@ IxLayout ix_layout(int n_max_rows, int max_tokens) {
   L.stages = stages > IX_MAX_STAGES ? IX_MAX_STAGES : stages;
   L.off_bar = L.off_raw + L.stages * IX_RAW;
   L.off_seg = L.off_bar + 512;
-  L.smem = L.off_seg + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  L.smem = L.off_seg + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 64 + 1024;
   L.acc_cols = 32;
   while (L.acc_cols < n_max_rows) L.acc_cols <<= 1;
   L.n_acc = IX_TMEM_COLS / L.acc_cols < IX_MAX_ACC ? IX_TMEM_COLS / L.acc_cols : IX_MAX_ACC;
@@ -139,6 +139,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   int32_t* s_w = reinterpret_cast<int32_t*>(segs + D.max_tokens);                    // [4][64], epilogue-owned
   int32_t* s_req = s_w + 4 * 64;                                                      // [n_tok]
   int32_t* s_lim = s_req + D.max_tokens;                                              // [n_tok]
+  int32_t* s_wsum = s_lim + D.max_tokens;                                             // [4][4], epilogue-owned
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hi = D.n_idx_heads;
@@ -318,17 +319,27 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
       if (!ok) *s_dead = 1;
       const uint8_t* raw = smem + L.off_raw + rs * IX_RAW;
       uint8_t* A = smem + ab * IX_A;
+      // chunk c -> (row, 16-byte piece): each group of 8 lanes takes pieces 0-3 of one
+      // row and pieces 4-7 of its neighbour, so its loads cover all 32 banks once and
+      // its two swizzled stores land on 8 distinct 16-byte slots (no bank conflicts)
+      auto piece_of = [](int c, int& row, int& ch16) {
+        const int half = (c >> 2) & 1;
+        row = 2 * (c >> 4) + (((c >> 3) & 1) ^ half);
+        ch16 = half * 4 + (c & 3);
+      };
       constexpr int CPT = IX_TILE * 8 / IX_CONV;   // 16-byte chunks per converter thread
       uint4 v[CPT];
 #pragma unroll
       for (int k = 0; k < CPT; ++k) {   // all loads first
-        const int c = ct + k * IX_CONV, row = c >> 3, ch16 = c & 7;
+        int row, ch16;
+        piece_of(ct + k * IX_CONV, row, ch16);
         v[k] = key0 + row < S.maxlim ? *reinterpret_cast<const uint4*>(raw + row * IDX_DIM + ch16 * 16)
                                      : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int k = 0; k < CPT; ++k) {
-        const int c = ct + k * IX_CONV, row = c >> 3, ch16 = c & 7;
+        int row, ch16;
+        piece_of(ct + k * IX_CONV, row, ch16);
         uint4 c0, c1;
         i8x16_to_f16(v[k], c0, c1);
         const int dim0 = ch16 * 16;
@@ -368,15 +379,23 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
           s_w[c] = w;
         }
         named_sync(2, 128);
+        if (tid < 16) {   // sum of the weights of each 16-head group, per token
+          int t = 0;
+          for (int k = 0; k < 16; ++k) t += s_w[(tid >> 2) * 64 + (tid & 3) * 16 + k];
+          s_wsum[tid] = t;
+        }
+        named_sync(2, 128);
         cur_seg = sg;
       }
       const int tb = i % L.n_acc;
       if (!mbar_wait(smem_u32(&t_full[tb]), (i / L.n_acc) & 1, D.status)) { *s_dead = 1; break; }
       tc_fence_after();
       // Exact integer epilogue without float->int conversions: every dot product
-      // is an integer |d| <= 2^21 held exactly in fp32, so max(d, 0) + 2^23 carries
-      // it in the low mantissa bits. With w <= 127, each w * relu(d) < 2^28 and 16
-      // of them sum below 2^32: 16 heads accumulate in uint32, the groups in 64 bits.
+      // is an integer |d| <= 2^21 held exactly in fp32, so max(d, 0) + 2^23 has the
+      // bit pattern 0x4B000000 + relu(d). With w <= 127, each w * relu(d) < 2^28 and
+      // 16 of them sum below 2^32: 16 heads accumulate bits * w in uint32 (mod 2^32)
+      // and the offset 0x4B000000 * sum(w) comes off once per group, which leaves the
+      // exact group sum; the groups add in 64 bits.
       for (int j = 0; j < S.ntok; ++j) {
         const int lim = s_lim[S.first + j];
         const uint32_t col0 = lane_base + (uint32_t)(tb * L.acc_cols + j * Hi);
@@ -389,7 +408,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           if (q * 16 < Hi) {
-            uint32_t s32 = 0;
+            uint32_t s32 = 0u - 0x4B000000u * (uint32_t)s_wsum[j * 4 + q];
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
               const int4 w4 = *reinterpret_cast<const int4*>(s_w + j * 64 + q * 16 + k4 * 4);
@@ -397,8 +416,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const float d = fmaxf(__uint_as_float(r[q * 16 + k4 * 4 + k]), 0.f);
-                const uint32_t u = __float_as_uint(d + 8388608.f) - 0x4B000000u;
-                s32 += u * (uint32_t)w[k];
+                s32 += __float_as_uint(d + 8388608.f) * (uint32_t)w[k];
               }
             }
             acc += s32;

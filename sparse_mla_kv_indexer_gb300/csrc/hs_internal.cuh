@@ -51,8 +51,6 @@ struct Dev {
   unsigned long long* counters;   // resident, hits, misses, h2d, d2h
   // scratch
   int64_t* scores;      // [max_tokens, max_ctx]
-  int4* miss_list;      // [max_tokens * topk] (layer-group row copies): {req, token, dst_row, 0}
-  int32_t* miss_count;  // [max_tokens] misses recorded by the segment starting at each token
   __half* o_part;       // [max_tokens, MAX_SPLITS, 512, 64] fp16 partial attention outputs
   float2* o_stats;      // [max_tokens, MAX_SPLITS, 64] per split and head: (max in log2 units, sum)
 };
@@ -97,13 +95,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// One bounded test of a phase: the warp may sleep in hardware until the phase
+// completes or the suspend hint (ns) expires, instead of spinning in issue slots.
+constexpr uint32_t MBAR_SUSPEND_NS = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(MBAR_SUSPEND_NS)
       : "memory");
   return ok != 0;
 }
@@ -113,7 +114,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 15u) == 0) {   // each test may sleep up to MBAR_SUSPEND_NS
       uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
@@ -327,8 +328,8 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
-inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                            int cluster_x, Args... args) {
+inline hs_status launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    dim3 cluster, Args... args) {
   cudaLaunchConfig_t lc = {};
   lc.gridDim = grid;
   lc.blockDim = block;
@@ -339,16 +340,22 @@ inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[na].val.programmaticStreamSerializationAllowed = 1;
   ++na;
-  if (cluster_x > 0) {
+  if (cluster.x * cluster.y * cluster.z > 1) {
     at[na].id = cudaLaunchAttributeClusterDimension;
-    at[na].val.clusterDim.x = cluster_x;
-    at[na].val.clusterDim.y = 1;
-    at[na].val.clusterDim.z = 1;
+    at[na].val.clusterDim.x = cluster.x;
+    at[na].val.clusterDim.y = cluster.y;
+    at[na].val.clusterDim.z = cluster.z;
     ++na;
   }
   lc.attrs = at;
   lc.numAttrs = na;
   return cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+// clusters of `cluster_x` CTAs along x (0: no cluster)
+template <typename... KArgs, typename... Args>
+inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            int cluster_x, Args... args) {
+  return launch_pdl_cluster(kernel, grid, block, smem, st, dim3(cluster_x > 0 ? cluster_x : 1, 1, 1), args...);
 }
 
 // ---- host-side launch helpers (defined in hs_pool.cu) ----------------------------

@@ -212,8 +212,6 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   chk(dev_alloc(p, &D.status, 1, 0));
   chk(dev_alloc(p, &D.counters, (size_t)C_N, 0));
   chk(dev_alloc(p, &D.scores, (size_t)c.max_tokens * c.max_ctx, 0));
-  chk(dev_alloc(p, &D.miss_list, (size_t)c.max_tokens * c.topk, 0));
-  chk(dev_alloc(p, &D.miss_count, (size_t)c.max_tokens, 0));
   chk(dev_alloc(p, &D.o_part, (size_t)c.max_tokens * MAX_SPLITS * 512 * 64, 0));
   chk(dev_alloc(p, &D.o_stats, (size_t)c.max_tokens * MAX_SPLITS * 64, 0));
   if (s == HS_OK) {

@@ -210,12 +210,12 @@ class BenchSession:
         self.d2h_bytes = self.out.numel() * self.out.element_size() if mode == "host" else 0
 
     def launches(self, i: int) -> int:
-        """Kernels one step launches: append; per indexer group the indexer and the
-        select kernel, the resolver and its miss copy; one attention kernel per
-        layer (the split merge runs inside it); offload when pages complete."""
+        """Kernels one step launches: append; per indexer group the indexer, the
+        select kernel and the resolver (which also copies its misses); one attention
+        kernel per layer (the split merge runs inside it); offload when pages complete."""
         cfg = self.run.cfg
         plan = self.steps[i][0]
-        return 1 + cfg.n_groups * 4 + cfg.n_layers + (1 if len(plan.offload) else 0)
+        return 1 + cfg.n_groups * 3 + cfg.n_layers + (1 if len(plan.offload) else 0)
 
     def tick(self, i: int) -> None:
         self.run.apply_tick(self.steps[i][0].tick)
