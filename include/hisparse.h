@@ -9,6 +9,8 @@
  *   hs_append_rows        write the step's new KV rows and index keys
  *   hs_indexer_topk       score every earlier token, keep the top K    [P2 "Why not TP or DP?"]
  *   hs_resolve_topk       map each selected token to a KV row id       [P1 "How it works"]
+ *   hs_replay_topk        the same row ids again, without touching the LRU state
+ *                         (verification reruns)                         [P1 "Composing with the rest of vLLM"]
  *   hs_sparse_mla_decode  attention over only those rows               [P2 footnote 1]
  *   hs_offload_pages      copy completed pages of all layers to host   [P1 "How it works"]
  *
@@ -60,7 +62,8 @@ typedef enum hs_status {
   HS_ERR_HOST_MISSING = 6, /* device: a placeholder page without a host copy was selected */
   HS_ERR_BAD_ID = 7,       /* device: a page, row or token id out of range */
   HS_ERR_BAD_WEIGHT = 8,   /* device: a negative index-head weight */
-  HS_ERR_SCRATCH_LIMIT = 9 /* request larger than the fixed scratch of hs_indexer_topk_noalloc */
+  HS_ERR_SCRATCH_LIMIT = 9, /* request larger than the fixed scratch of hs_indexer_topk_noalloc */
+  HS_ERR_NOT_RESOLVED = 10  /* hs_replay_topk met a token that is neither resident nor hot */
 } hs_status;
 
 /* Pool geometry. Sizes are fixed for the pool's lifetime. */
@@ -189,12 +192,27 @@ hs_status hs_resolve_topk(hs_pool* pool, int32_t group, int32_t step, int32_t n_
                           const int32_t* d_req, const int32_t* d_topk, int32_t* d_row_ids,
                           hs_plan_entry* d_plan, hs_stream_t stream);
 
+/* Replay of a resolver plan for a verification rerun ([P1] "Composing with the
+ * rest of vLLM": speculative decoding works through per-step replayable resolver
+ * plans that share the request's hot state). Maps each selected token to the row
+ * the last hs_resolve_topk of group `group` gave it, from the residency maps as
+ * they stand, and changes nothing: no LRU stamp is refreshed, no slot is taken, no
+ * row is copied, no counter moves. Every selected token must be resident or hold a
+ * hot slot (as right after hs_resolve_topk of the same selection); one that holds
+ * neither gets row id -1 and sets HS_ERR_NOT_RESOLVED in the device status word.
+ *  d_req [n], d_topk [n, K] as for hs_resolve_topk; d_row_ids [n, K] out (-1 for
+ *  pads). Graph-capturable; one launch. */
+hs_status hs_replay_topk(hs_pool* pool, int32_t group, int32_t n_tokens, const int32_t* d_req,
+                         const int32_t* d_topk, int32_t* d_row_ids, hs_stream_t stream);
+
 /* Sparse MLA decode for one layer ([P2] footnote 1; MQA form: every row serves
  * all heads). Per token and head: z_t = sm_scale * q . k_t over the 576 dims
  * (512 dequantised latent + 64 rope) of each selected row, o = softmax(z) . v_t
  * over the 512 latent dims, lse = log sum exp z.
- *  d_q [n, H, 576] bf16; d_row_ids [n, K] (-1 skipped); d_out [n, H, 512] bf16;
- *  d_lse nullable [n, H] fp32. */
+ *  d_q [n, H, 576] bf16, 16-byte aligned; d_row_ids [n, K] (-1 skipped);
+ *  d_out [n, H, 512] bf16, 16-byte aligned; d_lse nullable [n, H] fp32.
+ *  Per-group FP8 scales must be below 256 (HS_ERR_INVALID for misaligned
+ *  pointers or out-of-range arguments). */
 hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, int32_t n_tokens,
                                const uint16_t* d_q, const int32_t* d_row_ids, float sm_scale,
                                uint16_t* d_out, float* d_lse, hs_stream_t stream);

@@ -119,3 +119,33 @@ def resolve(topk_rows: np.ndarray, block_table: np.ndarray, hot: HotState, step:
         k, s, row, old = info[t]
         row_ids[idx], kind[idx], slot[idx], evicted[idx] = row, k, s, old
     return Resolution(row_ids, kind, slot, evicted, assigned, n_res, n_hit)
+
+
+class NotResolvedError(RuntimeError):
+    pass
+
+
+def replay(topk_rows: np.ndarray, block_table: np.ndarray, hot: HotState) -> np.ndarray:
+    """Replay of a resolver plan ("vLLM Part 1", section "Composing with the rest of
+    vLLM": speculative decoding works through per-step replayable resolver plans
+    that share the request's hot state).
+
+    Reading: a replay maps each selected token to the row the last resolve gave it,
+    from the residency maps as they stand, and changes nothing: no stamp is
+    refreshed, no victim is taken. A resident page gives its row in place, a token
+    holding a hot slot gives that slot's row; a token that is neither was not
+    resolved and is an error. Pads (-1) stay -1."""
+    topk_rows = np.asarray(topk_rows)
+    row_ids = np.full(topk_rows.shape, -1, np.int32)
+    for idx in np.ndindex(*topk_rows.shape):
+        t = int(topk_rows[idx])
+        if t < 0:
+            continue
+        p = t // PAGE
+        if block_table[p] >= 0:
+            row_ids[idx] = int(block_table[p]) * PAGE + t % PAGE
+        elif t in hot.tok2slot:
+            row_ids[idx] = hot.slot_row(hot.tok2slot[t])
+        else:
+            raise NotResolvedError(f"token {t} is neither resident nor in the hot buffer")
+    return row_ids

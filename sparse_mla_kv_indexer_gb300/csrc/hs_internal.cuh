@@ -366,6 +366,8 @@ hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const 
 hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* d_req,
                          const int32_t* d_topk, int32_t* d_row_ids, hs_plan_entry* d_plan,
                          cudaStream_t st);
+hs_status launch_replay(hs_pool* p, int group, int n, const int32_t* d_req, const int32_t* d_topk,
+                        int32_t* d_row_ids, cudaStream_t st);
 hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows,
                            float sm_scale, uint16_t* d_out, float* d_lse, cudaStream_t st);
 int num_sms();

@@ -140,6 +140,7 @@ const char* hs_status_string(hs_status s) {
     case HS_ERR_BAD_ID: return "page, row or token id out of range";
     case HS_ERR_BAD_WEIGHT: return "negative index-head weight";
     case HS_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation indexer";
+    case HS_ERR_NOT_RESOLVED: return "replayed token is neither resident nor in the hot buffer";
   }
   return "unknown status";
 }
@@ -321,11 +322,19 @@ hs_status hs_resolve_topk(hs_pool* p, int32_t group, int32_t step, int32_t n, co
   return launch_resolve(p, group, step, n, d_req, d_topk, d_row_ids, d_plan, reinterpret_cast<cudaStream_t>(stream));
 }
 
+hs_status hs_replay_topk(hs_pool* p, int32_t group, int32_t n, const int32_t* d_req, const int32_t* d_topk,
+                         int32_t* d_row_ids, hs_stream_t stream) {
+  if (!p || group < 0 || group >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  if (n == 0) return HS_OK;
+  if (!d_req || !d_topk || !d_row_ids) return HS_ERR_INVALID;
+  return launch_replay(p, group, n, d_req, d_topk, d_row_ids, reinterpret_cast<cudaStream_t>(stream));
+}
+
 hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, int32_t n, const uint16_t* d_q, const int32_t* d_row_ids,
                                float sm_scale, uint16_t* d_out, float* d_lse, hs_stream_t stream) {
   if (!p || layer < 0 || layer >= p->cfg.n_layers || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   if (n == 0) return HS_OK;
-  if (!d_q || !d_row_ids || !d_out || !aligned16(d_q) || (reinterpret_cast<uintptr_t>(d_out) & 7)) return HS_ERR_INVALID;
+  if (!d_q || !d_row_ids || !d_out || !aligned16(d_q) || !aligned16(d_out)) return HS_ERR_INVALID;
   return launch_attention(p, layer, n, d_q, d_row_ids, sm_scale, d_out, d_lse, reinterpret_cast<cudaStream_t>(stream));
 }
 

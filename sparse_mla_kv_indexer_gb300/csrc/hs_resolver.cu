@@ -477,4 +477,42 @@ hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* 
                             dim3(1, RS_COPY_CTAS, 1), p->d, group, step, n, d_req, d_topk, d_row_ids, d_plan);
 }
 
+// Replay: each (token, k) looked up in the residency maps as they stand; read only.
+__global__ void __launch_bounds__(256)
+replay_kernel(Dev D, int group, int n_tok, const int32_t* __restrict__ req_of, const int32_t* __restrict__ topk,
+              int32_t* __restrict__ row_ids) {
+  griddep_wait();
+  griddep_launch();
+  const int K = D.topk;
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (long long)n_tok * K) return;
+  const int j = (int)(e / K);
+  const int r = req_of[j];
+  const int t = topk[e];
+  int row = -1;
+  if (r < 0 || r >= D.max_requests || t >= D.max_ctx) {
+    set_status(D.status, HS_ERR_BAD_ID);
+  } else if (t >= 0) {
+    const size_t rg = (size_t)r * D.n_groups + group;
+    const int pg = D.bt[(size_t)r * D.max_pages + (t >> 6)];
+    if (pg >= 0 && pg < D.num_pages) {
+      row = pg * PAGE + (t & 63);
+    } else {
+      const int n_slots = min(D.n_hot[rg], D.hot_pages_max) * PAGE;
+      const int sl = D.tok2slot[rg * D.max_ctx + t];
+      const int hpage = (sl >= 0 && sl < n_slots) ? D.hot_pages[rg * D.hot_pages_max + (sl >> 6)] : -1;
+      if (hpage >= 0 && hpage < D.num_pages) row = hpage * PAGE + (sl & 63);
+      else set_status(D.status, HS_ERR_NOT_RESOLVED);
+    }
+  }
+  row_ids[e] = row;
+}
+
+hs_status launch_replay(hs_pool* p, int group, int n, const int32_t* d_req, const int32_t* d_topk, int32_t* d_row_ids,
+                        cudaStream_t st) {
+  const long long total = (long long)n * p->cfg.topk;
+  return launch_pdl(replay_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, st, 0, p->d, group, n, d_req,
+                    d_topk, d_row_ids);
+}
+
 }  // namespace hs

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhisparse
 STATUS = {
     0: "HS_OK", 1: "HS_ERR_INVALID", 2: "HS_ERR_OOM", 3: "HS_ERR_CAPACITY", 4: "HS_ERR_CUDA",
     5: "HS_ERR_TIMEOUT", 6: "HS_ERR_HOST_MISSING", 7: "HS_ERR_BAD_ID", 8: "HS_ERR_BAD_WEIGHT",
-    9: "HS_ERR_SCRATCH_LIMIT",
+    9: "HS_ERR_SCRATCH_LIMIT", 10: "HS_ERR_NOT_RESOLVED",
 }
 PLAN_PAD, PLAN_RESIDENT, PLAN_HIT, PLAN_MISS = 0, 1, 2, 3
 MAX_CTX = 1310720            # HS_MAX_CTX: longest context a pool accepts
@@ -57,6 +57,7 @@ _SIGS = {
     "hs_indexer_topk": [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P],
     "hs_indexer_topk_noalloc": [_P, _I, _I, _P, _P, _P, _P, _P, _P],
     "hs_resolve_topk": [_P, _I, _I, _I, _P, _P, _P, _P, _P],
+    "hs_replay_topk": [_P, _I, _I, _P, _P, _P, _P],
     "hs_sparse_mla_decode": [_P, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P],
     "hs_offload_pages": [_P, _I, _P, _P, _P],
     "hs_get_error": [_P, ctypes.POINTER(ctypes.c_int), _P],
@@ -168,6 +169,11 @@ class Pool:
     def resolve_topk(self, group: int, step: int, req, topk, row_ids, plan=None, stream=None) -> None:
         _check("hs_resolve_topk", lib.hs_resolve_topk(self.handle, group, step, req.numel(), _ptr(req), _ptr(topk),
                                                       _ptr(row_ids), _ptr(plan), _stream(stream)))
+
+    def replay_topk(self, group: int, req, topk, row_ids, stream=None) -> None:
+        """Row ids of an already resolved selection, without touching the LRU state."""
+        _check("hs_replay_topk", lib.hs_replay_topk(self.handle, group, req.numel(), _ptr(req), _ptr(topk),
+                                                    _ptr(row_ids), _stream(stream)))
 
     def sparse_mla_decode(self, layer: int, q, row_ids, sm_scale: float, out, lse=None, stream=None) -> None:
         _check("hs_sparse_mla_decode", lib.hs_sparse_mla_decode(self.handle, layer, q.shape[0], _ptr(q),

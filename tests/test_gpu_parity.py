@@ -113,3 +113,53 @@ def test_parity_tiny_all_pages_resident_no_misses():
         assert gpu.pool.counters().misses == 0
     finally:
         gpu.close()
+
+
+def test_replay_reproduces_the_resolved_rows_and_changes_no_state():
+    # multi-request MTP batch with misses, eviction and pool pressure; the oracle
+    # never replays, so any state a replay changed would show in the next step
+    cfg, wl, plans, oracle, gpu = _setup("small_batch")
+    import torch
+    try:
+        for plan in plans:
+            o = oracle.step(plan)
+            g = gpu.step(plan)
+            check_step(cfg, wl, plan, o, g, gpu, oracle)
+            req = torch.tensor([t.req for t in plan.tokens], dtype=torch.int32, device="cuda")
+            c0 = gpu.pool.counters()
+            for grp in range(cfg.n_groups):
+                topk = torch.from_numpy(np.ascontiguousarray(g["topk"][grp])).cuda()
+                rows = torch.full_like(topk, -7)
+                gpu.pool.replay_topk(grp, req, topk, rows)
+                assert np.array_equal(rows.cpu().numpy(), g["row_ids"][grp]), (plan.step, grp)
+            c1 = gpu.pool.counters()
+            assert (c0.resident, c0.hits, c0.misses, c0.h2d_bytes) == (c1.resident, c1.hits, c1.misses, c1.h2d_bytes)
+            assert gpu.pool.get_error() == 0
+    finally:
+        gpu.close()
+
+
+def test_replay_of_an_unresolved_token_reports_not_resolved():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_mla_kv_indexer_gb300 import hisparse as H
+    pc = H.PoolConfig(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=16, n_heads=16, topk=256,
+                      n_layers=1, layers_per_indexer=1, num_pages=4, num_idx_pages=4, max_requests=1,
+                      max_ctx=256, max_q_per_req=1, hot_rows=512, max_tokens=1, reserved=0, host_pages=4)
+    kv = [torch.zeros(4 * 64 * 656, dtype=torch.uint8, device="cuda")]
+    ix = [torch.zeros(4 * 64 * 128, dtype=torch.int8, device="cuda")]
+    host = torch.zeros(4 * 64 * 656, dtype=torch.uint8, pin_memory=True)
+    pool = H.Pool(pc, kv, ix, host)
+    try:
+        # page 0 resident at pool page 2, page 1 host-only and never resolved
+        pool.set_pages(0, 0, block_table=[2, -1], idx_pages=[0, 1], host_pages=[0, 1])
+        req = torch.zeros(1, dtype=torch.int32, device="cuda")
+        topk = torch.full((1, 256), -1, dtype=torch.int32, device="cuda")
+        topk[0, :3] = torch.tensor([5, 70, 63], dtype=torch.int32)
+        rows = torch.empty_like(topk)
+        pool.replay_topk(0, req, topk, rows)
+        assert pool.get_error() == 10   # HS_ERR_NOT_RESOLVED
+        assert rows[0, :4].cpu().tolist() == [2 * 64 + 5, -1, 2 * 64 + 63, -1]
+    finally:
+        pool.close()

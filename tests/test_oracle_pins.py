@@ -252,6 +252,37 @@ def test_resolver_mtp_union_resolves_once():
     assert res.row_ids.tolist() == [[576, 577, 578], [577, 578, 579]]
 
 
+def test_replay_follows_the_hand_worked_sequence_and_changes_nothing():
+    import copy
+    g = _load("resolver_hand.json")
+    bt = np.array(g["block_table"], np.int32)
+    hot = resolver.HotState()
+    hot.lease(g["hot_pages"])
+    for step, st in enumerate(g["steps"]):
+        sel = _sel(st["select"])
+        resolver.resolve(sel, bt, hot, step)
+        before = copy.deepcopy(hot)
+        rows = resolver.replay(sel, bt, hot)
+        pos = {int(t): i for i, t in enumerate(sel[0])}
+        for tok, (_, _, row, _) in st["expect"].items():
+            assert int(rows[0, pos[int(tok)]]) == row, (step, tok)
+        assert hot == before     # no stamp refreshed, no slot reassigned
+
+
+def test_replay_of_an_unresolved_or_evicted_token_is_an_error():
+    g = _load("resolver_hand.json")
+    bt = np.array(g["block_table"], np.int32)
+    hot = resolver.HotState()
+    hot.lease(g["hot_pages"])
+    with pytest.raises(resolver.NotResolvedError):      # nothing resolved yet
+        resolver.replay(np.array([[70]], np.int32), bt, hot)
+    assert resolver.replay(np.array([[0, 200, -1]], np.int32), bt, hot).tolist() == [[640, 712, -1]]
+    for step in range(2):                                # step 1 evicts token 96 (fixture)
+        resolver.resolve(_sel(g["steps"][step]["select"]), bt, hot, step)
+    with pytest.raises(resolver.NotResolvedError):
+        resolver.replay(np.array([[96]], np.int32), bt, hot)
+
+
 # ----------------------------------------------------------------------------
 # attention
 # ----------------------------------------------------------------------------
