@@ -154,7 +154,8 @@ class ClockSampler:
 def algorithmic_bytes(cfg, plans, counters_misses_rows):
     """Bytes each call must move at minimum, per call, averaged over the given steps.
 
-    indexer_topk: 128 B per scored key, keys read once per request (shared by its
+    indexer_topk: 128 B per scored key (132 B with FP8 keys: 128 values and a
+    scale, vLLM blog Part 2 footnote 3), keys read once per request (shared by its
     query tokens); sparse_mla_decode: per query token 2,048 rows x 660 B plus
     2,176 B of bf16 query and output per head (vLLM blog Part 2, footnote 1);
     resolve_topk: misses x 656 B x layers over the host link; offload_pages:
@@ -167,7 +168,7 @@ def algorithmic_bytes(cfg, plans, counters_misses_rows):
         keys += sum(per_req.values())
     keys /= len(plans)
     n_tok = len(plans[0].tokens)
-    idx = keys * 128
+    idx = keys * (132 if cfg.idx_fp8 else 128)
     attn = n_tok * (cfg.topk * 660 + cfg.n_heads * 2176)
     offl = sum(len(p.offload) for p in plans) / len(plans) * 64 * 656 * cfg.n_layers
     append = n_tok * (cfg.n_layers * 656 + cfg.n_groups * 128) * 2
@@ -229,8 +230,8 @@ def time_calls(torch, sess, i, flush, stream, reps=20):
     g0, l0 = 0, cfg.group_layers(0)[0]
     fns = {
         "append": lambda: pool.append_rows(d["req"], d["pos"], d["kv_rows"], d["idx_keys"]),
-        "indexer_topk": lambda: pool.indexer_topk(g0, d["req"], d["limit"], d["q_idx"][g0], d["w_idx"][g0],
-                                                  sess.topk[g0]),
+        "indexer_topk": lambda: sess.run.indexer_topk(g0, d["req"], d["limit"], d["q_idx"][g0], d["w_idx"][g0],
+                                                      sess.topk[g0]),
         "resolve_topk": lambda: pool.resolve_topk(g0, plan.step, d["req"], sess.topk[g0], sess.row_ids[g0]),
         "sparse_mla_decode": lambda: pool.sparse_mla_decode(l0, d["q_attn"][l0], sess.row_ids[g0],
                                                             sess.run.wl.sm_scale(), sess.out[l0]),

@@ -66,6 +66,17 @@ typedef enum hs_status {
   HS_ERR_NOT_RESOLVED = 10  /* hs_replay_topk met a token that is neither resident nor hot */
 } hs_status;
 
+/* Index-key formats.
+ * HS_IDX_INT8: 128 int8 values per key; a page of a key cache is [64][128] int8
+ *   (8,192 bytes); scores are exact int64 (hs_indexer_topk).
+ * HS_IDX_FP8: the pages' key record ([P2] footnote 3: 128 FP8 values plus a 4-byte
+ *   scale, 132 bytes): a page is 64 x 128 e4m3 bytes followed by the 64 keys' fp32
+ *   scales (8,448 bytes, HS_IDX_FP8_PAGE_BYTES); scores are fp32
+ *   (hs_indexer_topk_fp8). */
+#define HS_IDX_INT8 0
+#define HS_IDX_FP8 1
+#define HS_IDX_FP8_PAGE_BYTES 8448
+
 /* Pool geometry. Sizes are fixed for the pool's lifetime. */
 typedef struct hs_pool_config {
   int32_t page_size;          /* tokens per page; must be 64 */
@@ -83,7 +94,7 @@ typedef struct hs_pool_config {
   int32_t max_q_per_req;      /* query tokens per request per call, 1..4 */
   int32_t hot_rows;           /* hot-buffer capacity per (request, group), multiple of 64 */
   int32_t max_tokens;         /* query tokens per call, 1..1024 */
-  int32_t reserved;
+  int32_t idx_format;         /* index-key format: HS_IDX_INT8 or HS_IDX_FP8 */
   int64_t host_pages;         /* pages in the pinned host pool */
 } hs_pool_config;
 
@@ -113,8 +124,10 @@ typedef struct hs_pool hs_pool;
  *  d_kv_layers n_layers device pointers, each [num_pages, 64, 656] bytes, 16-byte aligned.
  *              Row layout: 512 FP8 e4m3 latent, 4 fp32 scales (one per 128 latent
  *              values), 64 bf16 rope values, little endian.
- *  d_idx_layers ceil(n_layers / layers_per_indexer) device pointers, each
- *              [num_idx_pages, 64, 128] int8 index keys, 16-byte aligned.
+ *  d_idx_layers ceil(n_layers / layers_per_indexer) device pointers, each a key
+ *              cache of num_idx_pages pages in cfg.idx_format's page layout
+ *              (HS_IDX_INT8: [64][128] int8; HS_IDX_FP8: [64][128] e4m3 then [64]
+ *              fp32 scales), 16-byte aligned.
  *  h_host_kv   pinned, mapped host memory of host_pages * n_layers * 64 * 656 bytes,
  *              layout [host_page][layer][64][656] (cudaHostAlloc or torch pin_memory).
  *  out         receives the pool.
@@ -161,7 +174,9 @@ hs_status hs_hot_release(hs_pool* pool, int32_t req, hs_stream_t stream);
 /* Write the KV row of every sparse layer and the index key of every indexer
  * layer for n_tokens new positions.
  *  d_req, d_pos   [n] request slot and position of each new row.
- *  d_kv_rows      [n, n_layers, 656] bytes; d_idx_keys [n, n_idx_layers, 128] int8.
+ *  d_kv_rows      [n, n_layers, 656] bytes; d_idx_keys [n, n_idx_layers, R] bytes,
+ *                 R = 128 (HS_IDX_INT8: int8 values) or 132 (HS_IDX_FP8: 128 e4m3
+ *                 values then the key's fp32 scale, little endian).
  * The page holding each position must be resident (block table >= 0). */
 hs_status hs_append_rows(hs_pool* pool, int32_t n_tokens, const int32_t* d_req,
                          const int32_t* d_pos, const uint8_t* d_kv_rows,
@@ -175,6 +190,19 @@ hs_status hs_append_rows(hs_pool* pool, int32_t n_tokens, const int32_t* d_req,
  *  ascending token order; -1 pads when limit < K.
  *  d_scores nullable [n, max_ctx] int64 out, 16-byte aligned: every score (entries >= limit
  *  undefined). */
+/* FP8 indexer and top-K for a pool with idx_format HS_IDX_FP8 ([P2] footnote 3:
+ * keys of 128 FP8 values and a 4-byte scale). Per query token j and earlier
+ * token t:
+ *   s[t] = scale_t * sum_h w[h] * max(0, sum_d q[h][d] * k_t[d])   (fp32)
+ * with q and k e4m3; a query's own scale is folded into its head weights w (fp32,
+ * any sign). The top K by (s descending, t ascending), ascending, -1 pads.
+ *  d_q [n, H_i, 128] e4m3, 16-byte aligned; d_w [n, H_i] fp32; d_topk [n, K] out;
+ *  d_scores nullable [n, max_ctx] fp32 out (entries >= limit untouched).
+ * HS_ERR_INVALID on a pool of the other format. */
+hs_status hs_indexer_topk_fp8(hs_pool* pool, int32_t index_layer, int32_t n_tokens, const int32_t* d_req,
+                              const int32_t* d_limit, const uint8_t* d_q, const float* d_w, int32_t* d_topk,
+                              float* d_scores, hs_stream_t stream);
+
 hs_status hs_indexer_topk(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
                           const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
                           const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,

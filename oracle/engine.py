@@ -28,7 +28,10 @@ class OracleRun:
         R = cfg.n_requests
         self.pool = [np.zeros((setup.num_pages * PAGE, 656), np.uint8) for _ in range(cfg.n_layers)]
         self.host = np.zeros((setup.host_pages, cfg.n_layers, PAGE, 656), np.uint8)
-        self.idx = [np.zeros((setup.num_idx_pages * PAGE, 128), np.int8) for _ in range(cfg.n_groups)]
+        # key cache rows: 128 int8 values, or the 132-byte FP8 record (codes + fp32 scale)
+        self.fp8 = bool(getattr(cfg, "idx_fp8", False))
+        self.idx = [np.zeros((setup.num_idx_pages * PAGE, 132 if self.fp8 else 128), np.uint8 if self.fp8 else np.int8)
+                    for _ in range(cfg.n_groups)]
         self.bt = setup.block_table.copy()
         self.hp = setup.host_page
         self.ip = setup.idx_page
@@ -46,7 +49,7 @@ class OracleRun:
                     if self.mat[r, p]:
                         self.host[self.hp[r, p], l, :hi - lo] = rows[lo:hi]
             for g in range(cfg.n_groups):
-                keys = wl.idx_keys(r, g)
+                keys = self.key_rows(r, g)
                 for p in range(-(-P // PAGE)):
                     lo, hi = p * PAGE, min(P, (p + 1) * PAGE)
                     b = int(self.ip[r, p]) * PAGE
@@ -74,7 +77,10 @@ class OracleRun:
                 self.pool[l][row] = self.wl.kv_rows(r, l)[pos]
             irow = int(self.ip[r, p]) * PAGE + off
             for g in range(self.cfg.n_groups):
-                self.idx[g][irow] = self.wl.idx_keys(r, g)[pos]
+                self.idx[g][irow] = self.key_rows(r, g)[pos]
+
+    def key_rows(self, r: int, g: int) -> np.ndarray:
+        return self.wl.idx_key_records_fp8(r, g) if self.fp8 else self.wl.idx_keys(r, g)
 
     def keys_of(self, g: int, r: int, n: int) -> np.ndarray:
         pos = np.arange(n)
@@ -96,10 +102,17 @@ class OracleRun:
             sc = []
             for i, t in enumerate(toks):
                 j = i % cfg.t_q   # tokens come grouped by request, t_q per request
-                q = wl.idx_queries(t.req, g, s)[j]
-                w = wl.idx_weights(t.req, g)
-                sv = indexer.scores(q, w, self.keys_of(g, t.req, t.limit))
-                tk[i] = indexer.topk(sv, K)
+                rows = self.keys_of(g, t.req, t.limit)
+                if self.fp8:
+                    qc, w = wl.idx_queries_fp8(t.req, g, s)
+                    scale = np.ascontiguousarray(rows[:, 128:132]).view("<f4").reshape(-1)
+                    sv = indexer.scores_fp8(qc[j], w[j], rows[:, :128], scale)
+                    tk[i] = indexer.topk_real(sv, K)
+                else:
+                    q = wl.idx_queries(t.req, g, s)[j]
+                    w = wl.idx_weights(t.req, g)
+                    sv = indexer.scores(q, w, rows)
+                    tk[i] = indexer.topk(sv, K)
                 if self.keep_scores:
                     sc.append(sv)
             row_ids = np.full((n, K), -1, np.int32)

@@ -13,6 +13,8 @@ ascending token order and padded with -1 when fewer than K tokens exist.
 """
 import numpy as np
 
+from . import formats
+
 
 def scores(q: np.ndarray, w: np.ndarray, keys: np.ndarray) -> np.ndarray:
     """q [H_i, 128] int8, w [H_i] int8, keys [n, 128] int8 -> [n] int64.
@@ -30,6 +32,31 @@ def topk(s: np.ndarray, k: int) -> np.ndarray:
     """Full sort of (-score, token) ascending; first min(k, n) tokens, ascending; -1 pads."""
     n = len(s)
     order = np.lexsort((np.arange(n), -np.asarray(s, np.int64)))
+    sel = np.sort(order[:min(k, n)])
+    out = np.full(k, -1, np.int32)
+    out[:len(sel)] = sel
+    return out
+
+
+def scores_fp8(q_codes: np.ndarray, w: np.ndarray, key_codes: np.ndarray, key_scales: np.ndarray) -> np.ndarray:
+    """FP8 keys as on the pages ("vLLM Part 2", footnote 3: 128 FP8 values plus a
+    4-byte scale per key).
+
+    q_codes [H_i, 128] e4m3 codes, w [H_i] fp32 head weights (the query's own scale
+    folded in, any sign), key_codes [n, 128] e4m3 codes, key_scales [n] fp32
+    -> [n] fp64:  s[t] = scale_t * sum_h w_h * max(0, sum_d q[h, d] * k_t[d]).
+    Reading: the scale multiplies the dequantised key; key scales are amax / 448 of
+    the key (never negative), so the scale may stand outside the ReLU."""
+    q = formats.e4m3_to_f64(np.asarray(q_codes, np.uint8))
+    k = formats.e4m3_to_f64(np.asarray(key_codes, np.uint8))
+    d = k @ q.T                                                       # [n, H_i]
+    return np.asarray(key_scales, np.float64) * (np.maximum(d, 0.0) @ np.asarray(w, np.float64))
+
+
+def topk_real(s: np.ndarray, k: int) -> np.ndarray:
+    """topk for real-valued scores: (-score, token) ascending, the same rule."""
+    n = len(s)
+    order = np.lexsort((np.arange(n), -np.asarray(s, np.float64)))
     sel = np.sort(order[:min(k, n)])
     out = np.full(k, -1, np.int32)
     out[:len(sel)] = sel

@@ -475,6 +475,13 @@ __device__ __forceinline__ int bucket1(unsigned long long v) {
   return 64 + (e - 6) * 64 + m;
 }
 
+// Level-0 bucket of a key. Integer scores (exact int64) span many octaves: log
+// buckets. Order-preserving keys of fp32 scores lie in one octave of the key space:
+// their top 12 bits (sign, exponent, 3 mantissa bits) are 4,096 monotone buckets.
+__device__ __forceinline__ int bucket_of(unsigned long long k, bool fp_keys) {
+  return fp_keys ? (int)(k >> 41) : bucket1(k);
+}
+
 // shared-memory histogram increment (scores spread over many buckets, so plain
 // atomics rarely collide within a warp)
 __device__ __forceinline__ void hist_add(uint32_t* hist, int bin) { atomicAdd(&hist[bin], 1u); }
@@ -524,7 +531,7 @@ __device__ void bitonic_desc(unsigned long long* a, int n) {
 template <int CL>
 __global__ void __launch_bounds__(SEL_THREADS, 1)
 select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of,
-              int32_t* __restrict__ topk) {
+              int32_t* __restrict__ topk, int fp_keys) {
   uint32_t crank_u;
   asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank_u));
   const int crank = (int)crank_u;
@@ -602,7 +609,7 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
       if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
       const unsigned long long k = ((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + i));
       cache[i] = k;
-      const int b = bucket1(k);
+      const int b = bucket_of(k, fp_keys);
       bk[i] = (uint16_t)b;
       hist_add(hist, b);
     }
@@ -628,7 +635,7 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
       for (int i = tid; i < cnt; i += blockDim.x) {
         long long v = (long long)piece[i];
         if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
-        const int b = bucket1(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + off + i)));
+        const int b = bucket_of(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + off + i)), fp_keys);
         bk[off + i] = (uint16_t)b;
         hist_add(hist, b);
       }
@@ -641,7 +648,8 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
     if (tid == 0 && (cnt_local & 1)) {
       long long v = s[lo + cnt_local - 1];
       if (v < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); v = 0; }
-      const int b = bucket1(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + cnt_local - 1)));
+      const int b = bucket_of(((unsigned long long)v << 21) | (IDX_MASK - (unsigned long long)(lo + cnt_local - 1)),
+                              fp_keys);
       bk[cnt_local - 1] = (uint16_t)b;
       hist_add(hist, b);
     }
@@ -735,7 +743,8 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   } else {
     // ---- slow path (crowded bucket): refine the key range level by level ----
     unsigned long long base, width;
-    if (B0 < 64) { base = B0; width = 1; }
+    if (fp_keys) { base = (unsigned long long)B0 << 41; width = 1ull << 41; }
+    else if (B0 < 64) { base = B0; width = 1; }
     else {
       int e = (B0 - 64) / 64 + 6, m = (B0 - 64) % 64;
       base = (1ull << e) + ((unsigned long long)m << (e - 6));
@@ -836,7 +845,7 @@ hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const 
 
 template <int CL>
 hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                           int32_t* d_topk, cudaStream_t st) {
+                           int32_t* d_topk, bool fp_keys, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(select_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_SMEM) !=
@@ -846,13 +855,13 @@ hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, con
     attr = true;
   }
   return launch_pdl(select_kernel<CL>, dim3(n * CL), dim3(SEL_THREADS), SEL_SMEM, st, CL, p->d, scores, ld, d_limit,
-                    d_topk);
+                    d_topk, fp_keys ? 1 : 0);
 }
 
 hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                        int32_t* d_topk, cudaStream_t st) {
+                        int32_t* d_topk, cudaStream_t st, bool fp_keys) {
   // 16 CTAs per token: each CTA's chunk is smaller and every pass shorter
-  return launch_select_cl<16>(p, n, scores, ld, d_limit, d_topk, st);
+  return launch_select_cl<16>(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
 }
 
 }  // namespace hs

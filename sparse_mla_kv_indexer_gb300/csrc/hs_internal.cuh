@@ -3,6 +3,7 @@
 // bulk copies, tcgen05 tensor-core and tensor-memory instructions).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -32,6 +33,7 @@ struct Dev {
   int32_t n_idx_heads, n_heads, topk, n_layers, lpi, n_groups;
   int32_t num_pages, num_idx_pages, max_requests, max_ctx, max_pages;
   int32_t max_q, hot_rows, hot_pages_max, max_tokens;
+  int32_t idx_fmt, idx_page_bytes;   // HS_IDX_INT8 / HS_IDX_FP8 and the key-cache page size
   int64_t host_pages;
   // residency metadata
   int32_t* bt;          // [max_requests, max_pages] pool page or -1
@@ -65,6 +67,7 @@ struct hs_pool {
   int device;
   std::vector<int32_t> n_hot_host;   // leased pages per (req, group), mirrored on the host
   std::vector<void*> allocations;
+  std::vector<CUtensorMap> idx_tmaps;   // HS_IDX_FP8: one per indexer layer, 128-byte swizzled key pages
 };
 
 namespace hs {
@@ -133,6 +136,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// 2-D tiled tensor load (TMA) of the box at (x, y) into shared memory, completing
+// bytes on `bar`; the tensor map is a __grid_constant__ kernel parameter.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -160,6 +171,15 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A . B with e4m3 operands (kind::f8f6f4; K = 32 per instruction).
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -241,6 +261,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
          | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16)
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// kind::f8f6f4 with e4m3 A and B (format code 0 in both operand fields) and f32 D:
+// the same bits as f16 x f16 -> f32; only the MMA's kind differs.
+__host__ __device__ constexpr uint32_t idesc_f8_e4m3(int M, int N) { return idesc_f16(M, N, false, false, false); }
 
 // ---- distributed shared memory (thread-block clusters) ---------------------------
 // Cluster-wide barrier with release/acquire ordering of shared-memory accesses.
@@ -361,11 +385,14 @@ inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 // ---- host-side launch helpers (defined in hs_pool.cu) ----------------------------
 hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
                          const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, cudaStream_t st);
+// fp_keys: the scores are order-preserving keys of fp32 scores (FP8 indexer)
 hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                        int32_t* d_topk, cudaStream_t st);
+                        int32_t* d_topk, cudaStream_t st, bool fp_keys = false);
 hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* d_req,
                          const int32_t* d_topk, int32_t* d_row_ids, hs_plan_entry* d_plan,
                          cudaStream_t st);
+hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
+                             const uint8_t* d_q, const float* d_w, int64_t* d_keys, float* d_scores, cudaStream_t st);
 hs_status launch_replay(hs_pool* p, int group, int n, const int32_t* d_req, const int32_t* d_topk,
                         int32_t* d_row_ids, cudaStream_t st);
 hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows,

@@ -46,7 +46,11 @@ __global__ void append_kernel(Dev D, int n, const int32_t* __restrict__ req_of, 
   griddep_wait();
   griddep_launch();
   const long long kv_chunks = (long long)n * D.n_layers * ROW_CHUNKS;
-  const long long ix_chunks = (long long)n * D.n_groups * (IDX_DIM / 16);
+  // key record per (token, group): 8 chunks of 16 bytes, plus the fp32 scale (HS_IDX_FP8)
+  const bool fp8 = D.idx_fmt == HS_IDX_FP8;
+  const int rec = fp8 ? 132 : IDX_DIM;
+  const int rec_parts = fp8 ? 9 : 8;
+  const long long ix_chunks = (long long)n * D.n_groups * rec_parts;
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < kv_chunks + ix_chunks;
        c += (long long)gridDim.x * blockDim.x) {
     if (c < kv_chunks) {
@@ -62,16 +66,23 @@ __global__ void append_kernel(Dev D, int n, const int32_t* __restrict__ req_of, 
       *reinterpret_cast<uint4*>(D.kv[layer] + ((size_t)pg * PAGE + (pos & 63)) * ROW + part * 16) = v;
     } else {
       const long long cc = c - kv_chunks;
-      const int part = (int)(cc % (IDX_DIM / 16));
-      const long long tg = cc / (IDX_DIM / 16);
+      const int part = (int)(cc % rec_parts);
+      const long long tg = cc / rec_parts;
       const int g = (int)(tg % D.n_groups);
       const int t = (int)(tg / D.n_groups);
       const int r = req_of[t], pos = pos_of[t];
       if (r < 0 || r >= D.max_requests || pos < 0 || pos >= D.max_ctx) { set_status(D.status, HS_ERR_BAD_ID); continue; }
       const int ip = D.idx_bt[(size_t)r * D.max_pages + (pos >> 6)];
       if (ip < 0 || ip >= D.num_idx_pages) { set_status(D.status, HS_ERR_BAD_ID); continue; }
-      const uint4 v = *reinterpret_cast<const uint4*>(idx_keys + ((size_t)t * D.n_groups + g) * IDX_DIM + part * 16);
-      *reinterpret_cast<uint4*>(D.idx[g] + ((size_t)ip * PAGE + (pos & 63)) * IDX_DIM + part * 16) = v;
+      const int8_t* src = idx_keys + ((size_t)t * D.n_groups + g) * rec;
+      int8_t* page = D.idx[g] + (size_t)ip * D.idx_page_bytes;
+      if (part < 8) {   // 128 key bytes (the FP8 record is only 4-byte aligned: copy by words)
+        const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src + part * 16);
+        *reinterpret_cast<uint4*>(page + (pos & 63) * IDX_DIM + part * 16) = make_uint4(s32[0], s32[1], s32[2], s32[3]);
+      } else {          // the key's fp32 scale, after the page's 64 keys
+        *reinterpret_cast<uint32_t*>(page + PAGE * IDX_DIM + (pos & 63) * 4) =
+            *reinterpret_cast<const uint32_t*>(src + IDX_DIM);
+      }
     }
   }
 }
@@ -145,6 +156,37 @@ const char* hs_status_string(hs_status s) {
   return "unknown status";
 }
 
+// HS_IDX_FP8 key caches as 2-D byte tensors of 128-byte rows (a page is 66 rows: 64
+// keys, then 2 rows of scales); the tensor load of one page's 64 key rows lands
+// 128-byte swizzled, the K-major operand layout of tcgen05.mma.
+static hs_status make_key_tensor_maps(hs_pool* p, void* const* d_idx_layers) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return HS_ERR_CUDA;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  p->idx_tmaps.resize(p->d.n_groups);
+  for (int g = 0; g < p->d.n_groups; ++g) {
+    const cuuint64_t dims[2] = {128, (cuuint64_t)p->cfg.num_idx_pages * (HS_IDX_FP8_PAGE_BYTES / 128)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, (cuuint32_t)PAGE};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&p->idx_tmaps[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d_idx_layers[g], dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return HS_ERR_INVALID;
+  }
+  return HS_OK;
+}
+
 hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void* const* d_idx_layers,
                        void* h_host_kv, hs_pool** out) {
   if (!cfg || !d_kv_layers || !d_idx_layers || !h_host_kv || !out) return HS_ERR_INVALID;
@@ -163,6 +205,7 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   if (c.max_q_per_req * c.n_idx_heads > 256) return HS_ERR_INVALID;
   if (c.hot_rows < PAGE || c.hot_rows % PAGE || c.hot_rows > 16384) return HS_ERR_INVALID;
   if (c.max_tokens < 1 || c.max_tokens > 1024 || c.host_pages < 1) return HS_ERR_INVALID;
+  if (c.idx_format != HS_IDX_INT8 && c.idx_format != HS_IDX_FP8) return HS_ERR_INVALID;
   const int n_groups = (c.n_layers + c.layers_per_indexer - 1) / c.layers_per_indexer;
   for (int l = 0; l < c.n_layers; ++l)
     if (!d_kv_layers[l] || !aligned16(d_kv_layers[l])) return HS_ERR_INVALID;
@@ -196,6 +239,8 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   D.max_tokens = c.max_tokens;
   D.host_pages = c.host_pages;
   D.host = static_cast<uint8_t*>(host_dev);
+  D.idx_fmt = c.idx_format;
+  D.idx_page_bytes = c.idx_format == HS_IDX_FP8 ? HS_IDX_FP8_PAGE_BYTES : IDX_PAGE_BYTES;
 
   const size_t R = c.max_requests, P = D.max_pages, G = n_groups;
   hs_status s = HS_OK;
@@ -221,6 +266,7 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
         cudaDeviceSynchronize() != cudaSuccess)
       s = HS_ERR_CUDA;
   }
+  if (s == HS_OK && c.idx_format == HS_IDX_FP8) s = make_key_tensor_maps(p, d_idx_layers);
   if (s != HS_OK) {
     hs_pool_destroy(p);
     return s;
@@ -307,11 +353,27 @@ hs_status hs_indexer_topk(hs_pool* p, int32_t index_layer, int32_t n, const int3
   if (n == 0) return HS_OK;
   if (!d_req || !d_limit || !d_q || !d_w || !d_topk || !aligned16(d_q)) return HS_ERR_INVALID;
   if (d_scores && !aligned16(d_scores)) return HS_ERR_INVALID;
+  if (p->d.idx_fmt != HS_IDX_INT8) return HS_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int64_t* scores = d_scores ? d_scores : p->d.scores;
   hs_status s = launch_indexer(p, index_layer, n, d_req, d_limit, d_q, d_w, scores, st);
   if (s != HS_OK) return s;
   return launch_select(p, n, scores, p->cfg.max_ctx, d_limit, d_topk, st);
+}
+
+hs_status hs_indexer_topk_fp8(hs_pool* p, int32_t index_layer, int32_t n, const int32_t* d_req,
+                              const int32_t* d_limit, const uint8_t* d_q, const float* d_w, int32_t* d_topk,
+                              float* d_scores, hs_stream_t stream) {
+  if (!p || index_layer < 0 || index_layer >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  if (n == 0) return HS_OK;
+  if (p->d.idx_fmt != HS_IDX_FP8) return HS_ERR_INVALID;
+  if (!d_req || !d_limit || !d_q || !d_w || !d_topk || !aligned16(d_q) || (reinterpret_cast<uintptr_t>(d_w) & 3))
+    return HS_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the kernel writes each score as an order-preserving integer for the selection
+  hs_status s = launch_indexer_fp8(p, index_layer, n, d_req, d_limit, d_q, d_w, p->d.scores, d_scores, st);
+  if (s != HS_OK) return s;
+  return launch_select(p, n, p->d.scores, p->cfg.max_ctx, d_limit, d_topk, st, true);
 }
 
 hs_status hs_resolve_topk(hs_pool* p, int32_t group, int32_t step, int32_t n, const int32_t* d_req,

@@ -33,7 +33,7 @@ def pool_config(wl: Workload, setup: Setup) -> H.PoolConfig:
         layers_per_indexer=cfg.layers_per_indexer, num_pages=setup.num_pages,
         num_idx_pages=setup.num_idx_pages, max_requests=cfg.n_requests, max_ctx=max_ctx,
         max_q_per_req=cfg.t_q, hot_rows=cfg.hot_rows, max_tokens=cfg.n_requests * cfg.t_q,
-        reserved=0, host_pages=setup.host_pages)
+        idx_format=H.IDX_FP8 if cfg.idx_fp8 else H.IDX_INT8, host_pages=setup.host_pages)
 
 
 class GpuRun:
@@ -51,7 +51,10 @@ class GpuRun:
         npg, nip = setup.num_pages, setup.num_idx_pages
         # host-side staging of the initial contents
         pool_np = [np.zeros((npg * PAGE, ROW_BYTES), np.uint8) for _ in range(L)]
-        idx_np = [np.zeros((nip * PAGE, IDX_DIM), np.int8) for _ in range(G)]
+        fp8 = cfg.idx_fp8
+        # key caches: int8 pages [64][128], or FP8 pages [64][128] e4m3 then [64] fp32 scales
+        idx_np = [np.zeros((nip, H.IDX_FP8_PAGE_BYTES), np.uint8) if fp8 else np.zeros((nip * PAGE, IDX_DIM), np.int8)
+                  for _ in range(G)]
         self.host = torch.zeros(setup.host_pages * L * PAGE * ROW_BYTES, dtype=torch.uint8, pin_memory=True)
         host_np = self.host.numpy().reshape(setup.host_pages, L, PAGE, ROW_BYTES)
         for r in range(R):
@@ -66,11 +69,17 @@ class GpuRun:
                     if setup.materialised[r, p]:
                         host_np[setup.host_page[r, p], l, :hi - lo] = rows[lo:hi]
             for g in range(G):
-                keys = wl.idx_keys(r, g)
+                if fp8:
+                    codes, scale = wl.idx_keys_fp8(r, g)
                 for p in range(-(-P // PAGE)):
                     lo, hi = p * PAGE, min(P, (p + 1) * PAGE)
-                    b = int(setup.idx_page[r, p]) * PAGE
-                    idx_np[g][b:b + hi - lo] = keys[lo:hi]
+                    ip = int(setup.idx_page[r, p])
+                    if fp8:
+                        page = idx_np[g][ip]
+                        page[:(hi - lo) * IDX_DIM] = codes[lo:hi].reshape(-1)
+                        page[PAGE * IDX_DIM:PAGE * IDX_DIM + 4 * (hi - lo)] = scale[lo:hi].astype("<f4").view(np.uint8)
+                    else:
+                        idx_np[g][ip * PAGE:ip * PAGE + hi - lo] = wl.idx_keys(r, g)[lo:hi]
         self.kv = [torch.from_numpy(a.reshape(-1)).to(self.dev) for a in pool_np]
         self.idx = [torch.from_numpy(a.reshape(-1)).to(self.dev) for a in idx_np]
         del pool_np, idx_np
@@ -101,17 +110,36 @@ class GpuRun:
             "pos": np.array([t.pos for t in toks], np.int32),
             "limit": np.array([t.limit for t in toks], np.int32),
             "kv_rows": np.stack([np.stack([wl.kv_rows(t.req, l)[t.pos] for l in range(cfg.n_layers)]) for t in toks]),
-            "idx_keys": np.stack([np.stack([wl.idx_keys(t.req, g)[t.pos] for g in range(cfg.n_groups)])
+            "idx_keys": np.stack([np.stack([self._key_record(t.req, g, t.pos) for g in range(cfg.n_groups)])
                                   for t in toks]),
-            "q_idx": np.stack([np.stack([wl.idx_queries(t.req, g, s)[i % t_q] for i, t in enumerate(toks)])
+            "q_idx": np.stack([np.stack([self._idx_query(t.req, g, s)[0][i % t_q] for i, t in enumerate(toks)])
                                for g in range(cfg.n_groups)]),
-            "w_idx": np.stack([np.stack([wl.idx_weights(t.req, g) for t in toks]) for g in range(cfg.n_groups)]),
+            "w_idx": np.stack([np.stack([self._idx_query(t.req, g, s)[1][i % t_q] for i, t in enumerate(toks)])
+                               for g in range(cfg.n_groups)]),
             "q_attn": np.stack([np.stack([wl.attn_queries(t.req, l, s)[i % t_q] for i, t in enumerate(toks)])
                                 for l in range(cfg.n_layers)]),
             "off_pool": np.array([o[2] for o in plan.offload], np.int32),
             "off_host": np.array([o[3] for o in plan.offload], np.int64),
         }
         return out
+
+    def _key_record(self, r: int, g: int, pos: int) -> np.ndarray:
+        """The key written for a new position: 128 int8, or the 132-byte FP8 record."""
+        return self.wl.idx_key_records_fp8(r, g)[pos] if self.cfg.idx_fp8 else self.wl.idx_keys(r, g)[pos]
+
+    def _idx_query(self, r: int, g: int, step: int):
+        """(index queries [t_q, H_i, 128], head weights [t_q, H_i]) in the pool's key format."""
+        if self.cfg.idx_fp8:
+            return self.wl.idx_queries_fp8(r, g, step)
+        w = self.wl.idx_weights(r, g)
+        return self.wl.idx_queries(r, g, step), np.broadcast_to(w, (self.cfg.t_q, w.shape[0]))
+
+    def indexer_topk(self, g, req, limit, q, w, topk, scores=None) -> None:
+        """The pool's indexer call for its key format."""
+        if self.cfg.idx_fp8:
+            self.pool.indexer_topk_fp8(g, req, limit, q, w, topk, scores)
+        else:
+            self.pool.indexer_topk(g, req, limit, q, w, topk, scores)
 
     def step(self, plan: StepPlan, collect: bool = True) -> Dict[str, object]:
         torch = self.torch
@@ -131,8 +159,9 @@ class GpuRun:
             q = torch.from_numpy(np.ascontiguousarray(x["q_idx"][g])).to(dev)
             w = torch.from_numpy(np.ascontiguousarray(x["w_idx"][g])).to(dev)
             topk = torch.empty((n, K), dtype=torch.int32, device=dev)
-            scores = torch.empty((n, self.max_ctx), dtype=torch.int64, device=dev) if self.keep_scores else None
-            self.pool.indexer_topk(g, req, limit, q, w, topk, scores)
+            sdt = torch.float32 if cfg.idx_fp8 else torch.int64
+            scores = torch.empty((n, self.max_ctx), dtype=sdt, device=dev) if self.keep_scores else None
+            self.indexer_topk(g, req, limit, q, w, topk, scores)
             row_ids = torch.empty((n, K), dtype=torch.int32, device=dev)
             plan_t = torch.empty((n, K, PLAN_FIELDS), dtype=torch.int32, device=dev)
             self.pool.resolve_topk(g, plan.step, req, topk, row_ids, plan_t)
@@ -243,8 +272,8 @@ class BenchSession:
                 d[k].copy_(host[k], non_blocking=True)
         timed("append", lambda: pool.append_rows(d["req"], d["pos"], d["kv_rows"], d["idx_keys"]))
         for g in range(cfg.n_groups):
-            timed("indexer_topk", lambda: pool.indexer_topk(g, d["req"], d["limit"], d["q_idx"][g], d["w_idx"][g],
-                                                            self.topk[g]))
+            timed("indexer_topk", lambda: run.indexer_topk(g, d["req"], d["limit"], d["q_idx"][g], d["w_idx"][g],
+                                                           self.topk[g]))
             timed("resolve_topk", lambda: pool.resolve_topk(g, plan.step, d["req"], self.topk[g], self.row_ids[g]))
             for l in cfg.group_layers(g):
                 timed("sparse_mla_decode", lambda: pool.sparse_mla_decode(l, d["q_attn"][l], self.row_ids[g],

@@ -19,6 +19,8 @@ STATUS = {
     9: "HS_ERR_SCRATCH_LIMIT", 10: "HS_ERR_NOT_RESOLVED",
 }
 PLAN_PAD, PLAN_RESIDENT, PLAN_HIT, PLAN_MISS = 0, 1, 2, 3
+IDX_INT8, IDX_FP8 = 0, 1       # HS_IDX_INT8, HS_IDX_FP8
+IDX_FP8_PAGE_BYTES = 8448      # 64 x 128 e4m3 key bytes, then 64 fp32 scales
 MAX_CTX = 1310720            # HS_MAX_CTX: longest context a pool accepts
 
 
@@ -32,7 +34,7 @@ class PoolConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "page_size", "row_bytes", "idx_dim", "n_idx_heads", "n_heads", "topk", "n_layers",
         "layers_per_indexer", "num_pages", "num_idx_pages", "max_requests", "max_ctx",
-        "max_q_per_req", "hot_rows", "max_tokens", "reserved")] + [("host_pages", ctypes.c_int64)]
+        "max_q_per_req", "hot_rows", "max_tokens", "idx_format")] + [("host_pages", ctypes.c_int64)]
 
 
 class PlanEntry(ctypes.Structure):
@@ -56,6 +58,7 @@ _SIGS = {
     "hs_append_rows": [_P, _I, _P, _P, _P, _P, _P],
     "hs_indexer_topk": [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P],
     "hs_indexer_topk_noalloc": [_P, _I, _I, _P, _P, _P, _P, _P, _P],
+    "hs_indexer_topk_fp8": [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P],
     "hs_resolve_topk": [_P, _I, _I, _I, _P, _P, _P, _P, _P],
     "hs_replay_topk": [_P, _I, _I, _P, _P, _P, _P],
     "hs_sparse_mla_decode": [_P, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P],
@@ -158,6 +161,12 @@ class Pool:
     def indexer_topk(self, index_layer: int, req, limit, q, w, topk, scores=None, stream=None) -> None:
         _check("hs_indexer_topk", lib.hs_indexer_topk(self.handle, index_layer, req.numel(), _ptr(req), _ptr(limit),
                                                       _ptr(q), _ptr(w), _ptr(topk), _ptr(scores), _stream(stream)))
+
+    def indexer_topk_fp8(self, index_layer: int, req, limit, q, w, topk, scores=None, stream=None) -> None:
+        """FP8 keys (pool idx_format IDX_FP8): q e4m3 bytes, w fp32, scores nullable fp32."""
+        _check("hs_indexer_topk_fp8", lib.hs_indexer_topk_fp8(self.handle, index_layer, req.numel(), _ptr(req),
+                                                              _ptr(limit), _ptr(q), _ptr(w), _ptr(topk), _ptr(scores),
+                                                              _stream(stream)))
 
     def indexer_topk_noalloc(self, index_layer: int, req, limit, q, w, topk, stream=None) -> None:
         """hs_indexer_topk with its score scratch in the library's fixed array, for

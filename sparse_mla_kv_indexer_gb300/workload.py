@@ -30,6 +30,7 @@ step to step. Query drift: q_t = clamp(q_{t-1} + round(N(0, 4^2))).
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -80,6 +81,7 @@ class WorkloadConfig:
     pool_slack_pages: int = 16        # free pool pages beyond what setup occupies
     prefix_reuse: Tuple[int, ...] = ()  # requests starting with placeholders + 1 hot page
     pressure: bool = False            # pool holds only the setup residency + slack: growth evicts
+    idx_fp8: bool = False             # index keys as 128 e4m3 values + an fp32 scale (132-byte record)
     seed: int = 0
 
     @property
@@ -153,6 +155,8 @@ def named_config(name: str) -> WorkloadConfig:
         return WorkloadConfig(name, 15, 3, (6000, 7000, 6500), topk=512, steps=5, t_q=4, accept=3,
                               tail_pages=4, host_only_frac=0.4, hot_rows=(3 + 2) * 512,
                               n_clusters=8, prefix_reuse=(2,), pressure=True)
+    if name.endswith("_fp8"):   # the same shape with FP8 index keys
+        return dataclasses.replace(named_config(name[:-4]), name=name, idx_fp8=True)
     if name == "short_ctx":
         # context shorter than K: every earlier token is selected, pads are -1
         return WorkloadConfig(name, 16, 2, (1500, 700), n_heads=16, n_idx_heads=16, topk=2048,
@@ -303,6 +307,34 @@ class Workload:
                 k[s:s + cfg.cluster_len] += cfg.cluster_bias * cl.dirs[c]
             self._ik[key] = np.clip(k, -127, 127).astype(np.int8)
         return self._ik[key]
+
+    def idx_keys_fp8(self, r: int, il: int):
+        """FP8 form of the same keys: ([final_len, 128] e4m3 codes, [final_len] fp32
+        scales), scale = amax / 448 per key (1 for an all-zero key)."""
+        key = ("fp8", r, il)
+        if key not in self._ik:
+            k = self.idx_keys(r, il).astype(np.float32)
+            amax = np.abs(k).max(axis=1)
+            scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+            self._ik[key] = (encode_e4m3(k / scale[:, None]), scale)
+        return self._ik[key]
+
+    def idx_key_records_fp8(self, r: int, il: int) -> np.ndarray:
+        """[final_len, 132] bytes: the e4m3 codes, then the scale (little-endian fp32)."""
+        codes, scale = self.idx_keys_fp8(r, il)
+        rec = np.empty((codes.shape[0], IDX_DIM + 4), np.uint8)
+        rec[:, :IDX_DIM] = codes
+        rec[:, IDX_DIM:] = scale.astype("<f4").view(np.uint8).reshape(-1, 4)
+        return rec
+
+    def idx_queries_fp8(self, r: int, il: int, step: int):
+        """FP8 form of a step's index queries: ([t_q, H_i, 128] e4m3 codes, [t_q, H_i]
+        fp32 weights); each head's scale amax / 448 is folded into its weight."""
+        q = self.idx_queries(r, il, step).astype(np.float32)
+        amax = np.abs(q).max(axis=2)
+        qs = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+        w = (self.idx_weights(r, il).astype(np.float32)[None, :] * qs).astype(np.float32)
+        return encode_e4m3(q / qs[:, :, None]), w
 
     def idx_weights(self, r: int, il: int) -> np.ndarray:
         """[H_i] int8 head weights, integers U[1, 16], fixed across steps."""

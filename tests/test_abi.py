@@ -62,7 +62,7 @@ def test_bad_geometry_is_invalid(lib):
     from sparse_mla_kv_indexer_gb300.hisparse import PoolConfig
     good = dict(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=64, n_heads=64, topk=2048,
                 n_layers=4, layers_per_indexer=4, num_pages=100, num_idx_pages=100, max_requests=1,
-                max_ctx=4096, max_q_per_req=1, hot_rows=4096, max_tokens=1, reserved=0, host_pages=10)
+                max_ctx=4096, max_q_per_req=1, hot_rows=4096, max_tokens=1, idx_format=0, host_pages=10)
     ptrs = (ctypes.c_void_p * 8)(*([16] * 8))
     out = ctypes.c_void_p()
     for key, bad in [("page_size", 32), ("row_bytes", 640), ("idx_dim", 64), ("n_heads", 48),

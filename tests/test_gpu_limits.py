@@ -8,7 +8,7 @@ pytestmark = pytest.mark.gpu
 def _pool(torch, H, max_ctx):
     pc = H.PoolConfig(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=16, n_heads=16, topk=256,
                       n_layers=1, layers_per_indexer=1, num_pages=4, num_idx_pages=4, max_requests=1,
-                      max_ctx=max_ctx, max_q_per_req=1, hot_rows=512, max_tokens=1, reserved=0, host_pages=1)
+                      max_ctx=max_ctx, max_q_per_req=1, hot_rows=512, max_tokens=1, idx_format=0, host_pages=1)
     kv = [torch.zeros(4 * 64 * 656, dtype=torch.uint8, device="cuda")]
     ix = [torch.zeros(4 * 64 * 128, dtype=torch.int8, device="cuda")]
     host = torch.zeros(64 * 656, dtype=torch.uint8, pin_memory=True)

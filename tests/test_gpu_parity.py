@@ -35,12 +35,13 @@ def _setup(name, **over):
     return cfg, wl, plans, oracle, gpu
 
 
-def check_step(cfg, wl, plan, o, g, gpu, oracle):
+def check_step(cfg, wl, plan, o, g, gpu, oracle, exact_scores=True):
     assert g["status"] == 0, f"device status {g['status']}"
     toks = plan.tokens
     for grp in range(cfg.n_groups):
         for i, t in enumerate(toks):
-            assert np.array_equal(g["scores"][grp][i, :t.limit], o["scores"][grp][i]), (plan.step, grp, i)
+            if exact_scores:
+                assert np.array_equal(g["scores"][grp][i, :t.limit], o["scores"][grp][i]), (plan.step, grp, i)
         assert np.array_equal(g["topk"][grp], o["topk"][grp]), (plan.step, grp)
         pg = g["plan"][grp]
         assert np.array_equal(g["row_ids"][grp], o["row_ids"][grp]), (plan.step, grp)
@@ -146,7 +147,7 @@ def test_replay_of_an_unresolved_token_reports_not_resolved():
     from sparse_mla_kv_indexer_gb300 import hisparse as H
     pc = H.PoolConfig(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=16, n_heads=16, topk=256,
                       n_layers=1, layers_per_indexer=1, num_pages=4, num_idx_pages=4, max_requests=1,
-                      max_ctx=256, max_q_per_req=1, hot_rows=512, max_tokens=1, reserved=0, host_pages=4)
+                      max_ctx=256, max_q_per_req=1, hot_rows=512, max_tokens=1, idx_format=0, host_pages=4)
     kv = [torch.zeros(4 * 64 * 656, dtype=torch.uint8, device="cuda")]
     ix = [torch.zeros(4 * 64 * 128, dtype=torch.int8, device="cuda")]
     host = torch.zeros(4 * 64 * 656, dtype=torch.uint8, pin_memory=True)

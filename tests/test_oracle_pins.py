@@ -411,3 +411,39 @@ def test_workload_rows_have_the_page_row_size():
     assert W.ROW_BYTES == closed_forms.row_bytes()
     assert cfg.hot_rows == 2 * cfg.topk
     assert W.named_config("batch32").hot_rows == (3 + 2) * 2048
+
+
+# ----------------------------------------------------------------------------
+# FP8 indexer keys
+# ----------------------------------------------------------------------------
+def test_fp8_scores_equal_the_exact_integer_scores_on_small_integers():
+    # integers of magnitude <= 16 are exact in e4m3; with unit scales the FP8 score
+    # must be the exact int64 score of the integer path (pinned above)
+    rng = np.random.default_rng(11)
+    q = rng.integers(-16, 17, size=(8, 128))
+    k = rng.integers(-16, 17, size=(300, 128))
+    w = rng.integers(1, 17, size=8)
+    ref = indexer.scores(q.astype(np.int8), w.astype(np.int8), k.astype(np.int8))
+    got = indexer.scores_fp8(W.encode_e4m3(q.astype(np.float32)), w.astype(np.float32),
+                             W.encode_e4m3(k.astype(np.float32)), np.ones(300, np.float32))
+    assert np.array_equal(got, ref.astype(np.float64))
+
+
+def test_fp8_scores_scale_with_the_key_scale_and_ignore_negative_dots():
+    rng = np.random.default_rng(12)
+    qc = W.encode_e4m3(rng.standard_normal((4, 128)).astype(np.float32))
+    kc = W.encode_e4m3(rng.standard_normal((50, 128)).astype(np.float32))
+    w = rng.standard_normal(4).astype(np.float32)
+    s1 = indexer.scores_fp8(qc, w, kc, np.ones(50, np.float32))
+    s3 = indexer.scores_fp8(qc, w, kc, np.full(50, 0.375, np.float32))
+    assert np.allclose(s3, 0.375 * s1, rtol=0, atol=1e-12)
+    # a key opposite to every query row scores 0 whatever the weights
+    qpos = np.full((4, 128), 0x38, np.uint8)    # e4m3 +1.0
+    neg = np.full((1, 128), 0xB8, np.uint8)     # e4m3 -1.0
+    assert np.all(indexer.scores_fp8(qpos, w, neg, np.ones(1, np.float32)) == 0.0)
+
+
+def test_topk_real_breaks_ties_toward_the_lower_token():
+    s = np.array([0.5, 2.0, 2.0, -1.0, 2.0, 0.5])
+    assert indexer.topk_real(s, 4).tolist() == [0, 1, 2, 4]
+    assert indexer.topk_real(s, 8).tolist() == [0, 1, 2, 3, 4, 5, -1, -1]

@@ -63,7 +63,7 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     max_ctx = 1 << 20                               # 4 tokens x 1M positions > 2^21 scores
     pc = H.PoolConfig(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=16, n_heads=16, topk=256,
                       n_layers=1, layers_per_indexer=1, num_pages=4, num_idx_pages=4, max_requests=1,
-                      max_ctx=max_ctx, max_q_per_req=4, hot_rows=512, max_tokens=4, reserved=0, host_pages=1)
+                      max_ctx=max_ctx, max_q_per_req=4, hot_rows=512, max_tokens=4, idx_format=0, host_pages=1)
     kv = [torch.zeros(4 * 64 * 656, dtype=torch.uint8, device="cuda")]
     ix = [torch.zeros(4 * 64 * 128, dtype=torch.int8, device="cuda")]
     host = torch.zeros(64 * 656, dtype=torch.uint8, pin_memory=True)
