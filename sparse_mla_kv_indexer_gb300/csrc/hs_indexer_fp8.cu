@@ -6,38 +6,47 @@
 //   s[t] = scale_t * sum_h w[h] * max(0, sum_d q[h][d] * k_t[d])      (fp32)
 // with q and k in e4m3 and the query's own scale folded into its head weights w.
 //
-// One persistent CTA per SM, six warps:
-//  * warp 4 (producer) fetches page ids 32 tiles ahead and loads each 128-key
+// One persistent CTA per SM, ten warps:
+//  * warp 8 (producer) fetches page ids 32 tiles ahead and loads each 128-key
 //    tile with two 2-D tensor loads (TMA), one per 64-key page: the e4m3 key rows
 //    land 128-byte swizzled, which is exactly the K-major operand layout of
 //    tcgen05.mma, so there is no conversion stage; the pages' 64 fp32 scales
-//    come with a 256-byte bulk copy each;
-//  * warp 5 issues tcgen05.mma kind::f8f6f4 (M = 128 keys, N = T * H_i, K = 128
-//    in four steps of 32) straight from the stage ring into up to 8 TMEM
-//    accumulators;
-//  * warps 0-3 (epilogue) load each request segment's queries (e4m3, swizzled)
-//    and weights, read the accumulators, form the fp32 score and store it as an
-//    order-preserving integer key for the top-K selection (and as fp32 when the
-//    caller asks), then release the accumulator and the stage.
+//    come with a 256-byte bulk copy each into a ring of their own, so that a key
+//    stage is free as soon as its MMAs complete (the MMA commit releases it) and
+//    only the small scale slot waits for the epilogue;
+//  * warp 9 puts each request segment's queries (e4m3, swizzled) in place, once
+//    its earlier MMAs have completed, and issues tcgen05.mma kind::f8f6f4 (M = 128
+//    keys, N = T * H_i, K = 128 in four steps of 32) straight from the stage ring
+//    into up to 8 TMEM accumulators;
+//  * warps 0-7 (epilogue, two warpgroups taking alternate tiles, so one tile's
+//    TMEM read and barrier latency overlaps the other's) read the accumulators,
+//    form the fp32 score and store it as an order-preserving integer key for the
+//    top-K selection (and as fp32 when the caller asks), then release the
+//    accumulator and the stage.
 #include "hs_internal.cuh"
 
 namespace hs {
 
-constexpr int F8_THREADS = 192;
-constexpr int F8_PRODUCER_WARP = 4, F8_MMA_WARP = 5;
+constexpr int F8_THREADS = 320;
+constexpr int F8_EPI_GROUPS = 2;                      // epilogue warpgroups
+constexpr int F8_PRODUCER_WARP = 8, F8_MMA_WARP = 9;
 constexpr int F8_TILE = 128;                          // keys per tile (two pages)
 constexpr int F8_KEY_BYTES = F8_TILE * IDX_DIM;       // 16 KB of e4m3 keys
-constexpr int F8_STAGE = 17 * 1024;                   // keys, then 128 fp32 scales; 1 KB aligned
-constexpr int F8_MAX_STAGES = 10;
+constexpr int F8_STAGE = F8_KEY_BYTES;                // a key stage; 1 KB aligned
+constexpr int F8_MAX_STAGES = 12;
+constexpr int F8_SC_SLOTS = 16;                       // scale ring: 128 fp32 per slot
+constexpr int F8_SC_BYTES = F8_SC_SLOTS * F8_TILE * 4;
 constexpr int F8_MAX_ACC = 8;
 constexpr int F8_TMEM_COLS = 512;
 constexpr int F8_BUDGET = 227 * 1024;
 constexpr int F8_PAGE_ROWS = HS_IDX_FP8_PAGE_BYTES / 128;   // a page is 66 rows of 128 bytes
-static_assert(F8_KEY_BYTES + F8_TILE * 4 <= F8_STAGE, "stage holds a tile and its scales");
+static_assert(F8_SC_SLOTS % 2 == 0, "each scale slot stays with one epilogue warpgroup");
+constexpr int F8_N_BARS = 2 * F8_MAX_STAGES + 2 * F8_MAX_ACC + 2 * F8_SC_SLOTS + 1;
+static_assert(F8_N_BARS * 8 + 32 <= 1024, "barriers and flags fit their region");
 
 struct F8Layout {
   int b_bytes;     // query operand [N][128] e4m3 (128-byte swizzled), 1 KB aligned
-  int off_stage, stages, off_bar, off_seg, smem;
+  int off_stage, stages, off_sc, off_bar, off_seg, smem;
   int acc_cols, n_acc;
 };
 
@@ -45,12 +54,13 @@ static F8Layout f8_layout(int n_max_rows, int max_tokens) {
   F8Layout L;
   L.b_bytes = (n_max_rows * 128 + 1023) & ~1023;
   L.off_stage = L.b_bytes;
-  const int tail = 512 + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  const int tail = F8_SC_BYTES + 1024 + max_tokens * 16 + F8_EPI_GROUPS * 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
   const int st = (F8_BUDGET - L.off_stage - tail) / F8_STAGE;
   L.stages = st > F8_MAX_STAGES ? F8_MAX_STAGES : st;
-  L.off_bar = L.off_stage + L.stages * F8_STAGE;
-  L.off_seg = L.off_bar + 512;
-  L.smem = L.off_seg + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  L.off_sc = L.off_stage + L.stages * F8_STAGE;
+  L.off_bar = L.off_sc + F8_SC_BYTES;
+  L.off_seg = L.off_bar + 1024;
+  L.smem = L.off_seg + max_tokens * 16 + F8_EPI_GROUPS * 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
   L.acc_cols = 32;
   while (L.acc_cols < n_max_rows) L.acc_cols <<= 1;
   L.n_acc = F8_TMEM_COLS / L.acc_cols < F8_MAX_ACC ? F8_TMEM_COLS / L.acc_cols : F8_MAX_ACC;
@@ -70,6 +80,15 @@ __device__ __forceinline__ long long f32_order_key(float x) {
 __device__ __forceinline__ void f8_named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+// Named barrier over n threads that also ORs a flag across them: every thread
+// leaves with the same answer, so an error seen by one thread ends the loop of all.
+__device__ __forceinline__ int f8_sync_or(int id, int n, int flag) {
+  int out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.s32 %0, 1, 0, q;\n}"
+      : "=r"(out) : "r"(flag), "r"(id), "r"(n) : "memory");
+  return out;
+}
 __device__ __forceinline__ void f8_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -85,18 +104,19 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
   uint8_t* Bq = smem;                                            // queries
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   uint64_t* full = bars;                                         // [NS] stage loaded
-  uint64_t* empty = bars + F8_MAX_STAGES;                        // [NS] stage released by the epilogue
+  uint64_t* empty = bars + F8_MAX_STAGES;                        // [NS] stage's MMAs completed
   uint64_t* t_full = bars + 2 * F8_MAX_STAGES;                   // [n_acc]
   uint64_t* t_empty = t_full + F8_MAX_ACC;                       // [n_acc]
-  uint64_t* b_full = t_empty + F8_MAX_ACC;                       // [1] a segment's queries are in place
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
+  uint64_t* c_full = t_empty + F8_MAX_ACC;                       // [F8_SC_SLOTS] scales loaded
+  uint64_t* c_empty = c_full + F8_SC_SLOTS;                      // [F8_SC_SLOTS] scales read by the epilogue
+  uint64_t* b_done = c_empty + F8_SC_SLOTS;                      // [1] MMAs reading the queries completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_done + 1);
   int32_t* s_nseg = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* s_dead = s_nseg + 1;
   int32_t* s_issued = s_nseg + 2;
-  int32_t* s_consumed = s_nseg + 3;
   F8Seg* segs = reinterpret_cast<F8Seg*>(smem + L.off_seg);
-  float* s_w = reinterpret_cast<float*>(segs + D.max_tokens);     // [4][64]
-  int32_t* s_req = reinterpret_cast<int32_t*>(s_w + 4 * 64);      // [n_tok]
+  float* s_w = reinterpret_cast<float*>(segs + D.max_tokens);     // [F8_EPI_GROUPS][4][64]
+  int32_t* s_req = reinterpret_cast<int32_t*>(s_w + F8_EPI_GROUPS * 4 * 64);   // [n_tok]
   int32_t* s_lim = s_req + D.max_tokens;                          // [n_tok]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -105,7 +125,7 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
 
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), F8_TMEM_COLS);
   if (tid == 0) {
-    for (int b = 0; b < 2 * F8_MAX_STAGES + 2 * F8_MAX_ACC + 1; ++b) mbar_init(smem_u32(&bars[b]), 1);
+    for (int b = 0; b < F8_N_BARS; ++b) mbar_init(smem_u32(&bars[b]), 1);
     fence_mbar_init();
   }
   griddep_wait();
@@ -142,7 +162,6 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     *s_nseg = ns;
     *s_dead = 0;
     *s_issued = 0;
-    *s_consumed = 0;
   }
   tc_fence_before();
   __syncthreads();
@@ -188,25 +207,29 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
       const int ip1 = __shfl_sync(0xffffffffu, c1, i & 31);
       int dead = 0;
       if (lane == 0) {
-        const int rs = i % NS;
-        if (i >= NS && !mbar_wait(smem_u32(&empty[rs]), ((i / NS) - 1) & 1, D.status)) *s_dead = 1;
+        const int rs = i % NS, cs = i % F8_SC_SLOTS;
+        if (i >= NS && !mbar_wait_spin(smem_u32(&empty[rs]), ((i / NS) - 1) & 1, D.status)) *s_dead = 1;
+        if (i >= F8_SC_SLOTS && !mbar_wait_spin(smem_u32(&c_empty[cs]), ((i / F8_SC_SLOTS) - 1) & 1, D.status))
+          *s_dead = 1;
         dead = *(volatile int32_t*)s_dead;
         if (!dead) {
-          const uint32_t bar = smem_u32(&full[rs]);
+          const uint32_t bar = smem_u32(&full[rs]), cbar = smem_u32(&c_full[cs]);
           uint8_t* stage = smem + L.off_stage + rs * F8_STAGE;
+          uint8_t* slot = smem + L.off_sc + cs * F8_TILE * 4;
           const int ips[2] = {ip0, ip1};
           uint32_t bytes = 0;
           for (int k = 0; k < 2; ++k) {
             if (ips[k] == -2) continue;
             if (ips[k] < 0 || ips[k] >= D.num_idx_pages) { set_status(D.status, HS_ERR_BAD_ID); continue; }
-            bytes += PAGE * IDX_DIM + PAGE * 4;
+            bytes += PAGE * IDX_DIM;
           }
           mbar_expect_tx(bar, bytes);
+          mbar_expect_tx(cbar, bytes / IDX_DIM * 4);
           for (int k = 0; k < 2; ++k)
             if (ips[k] >= 0 && ips[k] < D.num_idx_pages) {
               tma_load_2d(smem_u32(stage + k * PAGE * IDX_DIM), &tmap, 0, ips[k] * F8_PAGE_ROWS, bar);
-              bulk_g2s(smem_u32(stage + F8_KEY_BYTES + k * PAGE * 4),
-                       keys + (size_t)ips[k] * HS_IDX_FP8_PAGE_BYTES + PAGE * IDX_DIM, PAGE * 4, bar);
+              bulk_g2s(smem_u32(slot + k * PAGE * 4),
+                       keys + (size_t)ips[k] * HS_IDX_FP8_PAGE_BYTES + PAGE * IDX_DIM, PAGE * 4, cbar);
             }
           *s_issued = i + 1;
         }
@@ -215,55 +238,25 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     }
   } else if (warp == F8_MMA_WARP) {
     // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0) {
-      int cur_seg = -1, nb = 0;
-      for (int i = 0; i < n_local; ++i) {
-        const int rs = i % NS, tb = i % L.n_acc;
-        const int sg = seg_of(item_of(i));
-        bool ok = true;
-        if (sg != cur_seg) {   // this segment's queries are in place
-          ok = mbar_wait(smem_u32(b_full), nb & 1, D.status);
-          ++nb;
-          cur_seg = sg;
-        }
-        if (ok) ok = mbar_wait(smem_u32(&full[rs]), (i / NS) & 1, D.status);
-        if (ok && i >= L.n_acc) ok = mbar_wait(smem_u32(&t_empty[tb]), ((i / L.n_acc) - 1) & 1, D.status);
-        if (!ok || *(volatile int32_t*)s_dead) { *s_dead = 1; break; }
-        tc_fence_after();
-        const int N = ((segs[sg].ntok * Hi) + 15) & ~15;
-        const uint32_t idesc = idesc_f8_e4m3(128, N);
-        const uint32_t a0 = smem_u32(smem + L.off_stage + rs * F8_STAGE), b0 = smem_u32(Bq);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // K = 128 e4m3 = one 128-byte swizzle atom, 32 per step
-          const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(b0 + kk * 32, 16, 1024);
-          umma_f8(tmem + tb * L.acc_cols, ad, bd, idesc, kk > 0);
-        }
-        umma_commit(smem_u32(&t_full[tb]));
-      }
-    }
-  } else if (warp < 4) {
-    // ------------------------------ epilogue ------------------------------
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    int cur_seg = -1;
+    // lane 0 waits and issues; the warp's 32 lanes load each segment's queries
+    int cur_seg = -1, nb = 0, any = 0;
     for (int i = 0; i < n_local; ++i) {
-      const int item = item_of(i);
-      const int sg = seg_of(item);
-      const F8Seg S = segs[sg];
-      const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
-      const int row = tid;                       // TMEM lane = key row of the tile
-      const int key = tile * F8_TILE + row;
       const int rs = i % NS, tb = i % L.n_acc;
+      const int sg = seg_of(item_of(i));
+      int ok = 1;
       if (sg != cur_seg) {
-        // every MMA of earlier tiles has completed (their accumulators were read),
-        // so the query operand may be replaced
-        f8_named_sync(2, 128);
-        for (int c = tid; c < 4 * 64; c += 128) {
-          const int j = c >> 6, h = c & 63;
-          s_w[c] = (j < S.ntok && h < Hi) ? wg[(size_t)(S.first + j) * Hi + h] : 0.f;
+        if (i > 0) {   // the previous segment's MMAs still read the query operand
+          if (lane == 0) {
+            umma_commit(smem_u32(b_done));
+            ok = mbar_wait_spin(smem_u32(b_done), nb & 1, D.status);
+          }
+          ++nb;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) { *s_dead = 1; break; }
         }
+        const F8Seg S = segs[sg];
         const int N = ((S.ntok * Hi) + 15) & ~15;
-        for (int c = tid; c < N * 8; c += 128) {
+        for (int c = lane; c < N * 8; c += 32) {
           const int r = c >> 3, ch = c & 7;
           uint4 v = make_uint4(0, 0, 0, 0);
           if (r < S.ntok * Hi) {
@@ -273,16 +266,69 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
           *reinterpret_cast<uint4*>(Bq + sw128_chunk(r, ch)) = v;
         }
         fence_proxy_async();
-        f8_named_sync(2, 128);
-        if (tid == 0) f8_arrive(smem_u32(b_full));
+        __syncwarp();
         cur_seg = sg;
       }
-      if (!mbar_wait(smem_u32(&t_full[tb]), (i / L.n_acc) & 1, D.status)) { *s_dead = 1; break; }
-      // the stage's bulk copies (the scales) are complete and visible here too; the
-      // stage cannot be refilled before this tile releases it, so its phase is this tile's
-      if (!mbar_wait(smem_u32(&full[rs]), (i / NS) & 1, D.status)) { *s_dead = 1; break; }
+      if (lane == 0) {
+        ok = mbar_wait_spin(smem_u32(&full[rs]), (i / NS) & 1, D.status);
+        if (ok && i >= L.n_acc) ok = mbar_wait_spin(smem_u32(&t_empty[tb]), ((i / L.n_acc) - 1) & 1, D.status);
+        if (ok && !*(volatile int32_t*)s_dead) {
+          tc_fence_after();
+          const int N = ((segs[sg].ntok * Hi) + 15) & ~15;
+          const uint32_t idesc = idesc_f8_e4m3(128, N);
+          const uint32_t a0 = smem_u32(smem + L.off_stage + rs * F8_STAGE), b0 = smem_u32(Bq);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {   // K = 128 e4m3 = one 128-byte swizzle atom, 32 per step
+            const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + kk * 32, 16, 1024);
+            umma_f8(tmem + tb * L.acc_cols, ad, bd, idesc, kk > 0);
+          }
+          umma_commit(smem_u32(&t_full[tb]));
+          umma_commit(smem_u32(&empty[rs]));        // the key stage is free once these MMAs complete
+          any = 1;
+        } else {
+          ok = 0;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) { *s_dead = 1; break; }
+    }
+    if (lane == 0 && any && *(volatile int32_t*)s_dead) {
+      // the epilogue may have stopped early: let the MMAs in flight finish before TMEM is freed
+      umma_commit(smem_u32(b_done));
+      mbar_wait_spin(smem_u32(b_done), nb & 1, D.status);
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int grp = warp >> 2, et = tid & 127;          // warpgroup, thread within it
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    float* sw = s_w + grp * 4 * 64;
+    int cur_seg = -1;
+    for (int i = grp; i < n_local; i += F8_EPI_GROUPS) {
+      const int item = item_of(i);
+      const int sg = seg_of(item);
+      const F8Seg S = segs[sg];
+      const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
+      const int row = et;                        // TMEM lane = key row of the tile
+      const int key = tile * F8_TILE + row;
+      const int cs = i % F8_SC_SLOTS, tb = i % L.n_acc;
+      if (sg != cur_seg) {
+        f8_named_sync(2 + grp, 128);
+        for (int c = et; c < 4 * 64; c += 128) {
+          const int j = c >> 6, h = c & 63;
+          sw[c] = (j < S.ntok && h < Hi) ? wg[(size_t)(S.first + j) * Hi + h] : 0.f;
+        }
+        f8_named_sync(2 + grp, 128);
+        cur_seg = sg;
+      }
+      // a failed wait is recorded and the tile run through without stores, so that the
+      // warpgroup's decision to stop is taken together at the barrier below
+      int ok = mbar_wait_spin(smem_u32(&t_full[tb]), (i / L.n_acc) & 1, D.status);
+      // a scale slot is refilled only after this warpgroup releases it, so its phase is this tile's
+      ok = ok && mbar_wait_spin(smem_u32(&c_full[cs]), (i / F8_SC_SLOTS) & 1, D.status);
+      if (!ok) *s_dead = 1;
       tc_fence_after();
-      const float scale = *reinterpret_cast<const float*>(smem + L.off_stage + rs * F8_STAGE + F8_KEY_BYTES + row * 4);
+      const float scale = *reinterpret_cast<const float*>(smem + L.off_sc + cs * F8_TILE * 4 + row * 4);
       for (int j = 0; j < S.ntok; ++j) {
         const int lim = s_lim[S.first + j];
         const uint32_t col0 = lane_base + (uint32_t)(tb * L.acc_cols + j * Hi);
@@ -291,38 +337,40 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
         for (int q = 0; q < 4; ++q)
           if (q * 16 < Hi) tmem_ld16(col0 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(r + q * 16));
         tmem_wait_ld();
-        float acc = 0.f;
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};      // four independent chains
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           if (q * 16 < Hi) {
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-              const float4 w4 = *reinterpret_cast<const float4*>(s_w + j * 64 + q * 16 + k4 * 4);
+              const float4 w4 = *reinterpret_cast<const float4*>(sw + j * 64 + q * 16 + k4 * 4);
               const float w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-              for (int k = 0; k < 4; ++k) acc = fmaf(w[k], fmaxf(__uint_as_float(r[q * 16 + k4 * 4 + k]), 0.f), acc);
+              for (int k = 0; k < 4; ++k) a4[k] = fmaf(w[k], fmaxf(__uint_as_float(r[q * 16 + k4 * 4 + k]), 0.f), a4[k]);
             }
           }
-        const float s = acc * scale + 0.f;     // + 0: a zero score is +0 whatever the signs
-        if (key < lim) {
+        const float s = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * scale + 0.f;   // + 0: a zero score is +0
+        if (ok && key < lim) {
           keys_out[(size_t)(S.first + j) * ld + key] = f32_order_key(s);
           if (scores_out) scores_out[(size_t)(S.first + j) * ld + key] = s;
         }
       }
       tc_fence_before();
-      f8_named_sync(2, 128);
-      if (tid == 0) {
+      const int dead = f8_sync_or(2 + grp, 128, *(volatile int32_t*)s_dead);
+      if (dead) break;
+      if (et == 0) {
         f8_arrive(smem_u32(&t_empty[tb]));
-        f8_arrive(smem_u32(&empty[rs]));
-        *s_consumed = i + 1;
+        f8_arrive(smem_u32(&c_empty[cs]));
       }
-      if (*(volatile int32_t*)s_dead) break;
     }
   }
   __syncthreads();
   if (*s_dead && tid == F8_PRODUCER_WARP * 32) {
-    // drain bulk copies still in flight before the CTA's shared memory goes away
-    for (int k = *s_consumed; k < *s_issued; ++k) mbar_wait(smem_u32(&full[k % NS]), (k / NS) & 1, D.status);
+    // drain the copies that may still be in flight (the last use of every stage
+    // and scale slot) before the CTA's shared memory goes away
+    for (int k = max(0, *s_issued - NS); k < *s_issued; ++k) mbar_wait_spin(smem_u32(&full[k % NS]), (k / NS) & 1, D.status);
+    for (int k = max(0, *s_issued - F8_SC_SLOTS); k < *s_issued; ++k)
+      mbar_wait_spin(smem_u32(&c_full[k % F8_SC_SLOTS]), (k / F8_SC_SLOTS) & 1, D.status);
   }
   tc_fence_before();
   __syncthreads();
@@ -335,7 +383,9 @@ hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, co
                              cudaStream_t st) {
   const int n_max = ((p->cfg.max_q_per_req * p->cfg.n_idx_heads) + 15) & ~15;
   const F8Layout L = f8_layout(n_max, p->cfg.max_tokens);
-  if (L.stages < 2 || il < 0 || il >= (int)p->idx_tmaps.size()) return HS_ERR_INVALID;
+  // alternate tiles go to alternate epilogue warpgroups: an even accumulator count
+  // keeps every accumulator with one warpgroup, so its phase waits never alias
+  if (L.stages < 2 || L.n_acc % F8_EPI_GROUPS || il < 0 || il >= (int)p->idx_tmaps.size()) return HS_ERR_INVALID;
   static int attr_smem = 0;
   if (attr_smem < L.smem) {
     if (cudaFuncSetAttribute(indexer_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem) != cudaSuccess)

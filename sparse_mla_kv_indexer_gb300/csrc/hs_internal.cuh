@@ -129,6 +129,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   }
 }
 
+// The same wait polling without the suspend hint: for a short pipeline whose
+// phases complete within a few hundred ns, a hardware sleep wakes up later than
+// polling notices the phase.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, int32_t* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 255u) == 0) {
+      uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > WAIT_NS) {
+        set_status(status, HS_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ---- bulk copies (TMA unit, untiled) ------------------------------------------
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
