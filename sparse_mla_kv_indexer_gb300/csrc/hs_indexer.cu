@@ -27,7 +27,7 @@
 // each CTA then emits its selected tokens in ascending order at its offset.
 #include <cooperative_groups.h>
 
-#include "hs_internal.cuh"
+#include "hs_select.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -443,14 +443,9 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
 }
 
 // ----------------------------------------------------------------------------------
-// Select kernel
+// Select kernel (one cluster per query token); keys as in hs_select.cuh
 // ----------------------------------------------------------------------------------
-// Each score s of token index t is made unique and order-preserving as the key
-//   key = s * 2^21 + (2^21 - 1 - t)          (s >= 0, t < 2^21)
-// so the top K by (score desc, token asc) are exactly the K largest keys, and the
-// K-th largest key tau selects them with the single test key >= tau.
 constexpr int SEL_THREADS = 512;
-constexpr int SEL_BINS = 4096;
 constexpr int SEL_CACHE = 12288;                       // keys cached in shared memory per CTA
 constexpr int SEL_CAND = 2048;                         // candidates per CTA on the fast path
 constexpr int SEL_LEAD = 4096;                         // candidates the cluster leader sorts
@@ -465,52 +460,10 @@ constexpr int SEL_SMEM_CACHED = SEL_CACHE * 8 + SEL_CACHE * 2 + SEL_LEAD * 8 + S
 constexpr int SEL_SMEM_STREAM = SEL_STREAM_MAX * 2 + SEL_RING * SEL_PIECE * 8;
 constexpr int SEL_SMEM = (SEL_SMEM_CACHED > SEL_SMEM_STREAM ? SEL_SMEM_CACHED : SEL_SMEM_STREAM) + 16;
 static_assert(SEL_LEAD * 8 + SEL_CAND * 8 <= SEL_RING * SEL_PIECE * 8, "lead and cand fit in the ring");
-constexpr unsigned long long IDX_MASK = (1ull << 21) - 1;
-
-// monotone level-0 bucket of a key: exact below 64, then 64 buckets per octave
-__device__ __forceinline__ int bucket1(unsigned long long v) {
-  if (v < 64) return (int)v;
-  int e = 63 - __clzll((long long)v);
-  int m = (int)((v >> (e - 6)) & 63);
-  return 64 + (e - 6) * 64 + m;
-}
-
-// Level-0 bucket of a key. Integer scores (exact int64) span many octaves: log
-// buckets. Order-preserving keys of fp32 scores lie in one octave of the key space:
-// their top 12 bits (sign, exponent, 3 mantissa bits) are 4,096 monotone buckets.
-__device__ __forceinline__ int bucket_of(unsigned long long k, bool fp_keys) {
-  return fp_keys ? (int)(k >> 41) : bucket1(k);
-}
 
 // shared-memory histogram increment (scores spread over many buckets, so plain
 // atomics rarely collide within a warp)
 __device__ __forceinline__ void hist_add(uint32_t* hist, int bin) { atomicAdd(&hist[bin], 1u); }
-
-__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int t = lane < nw ? warp_tot[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    if (lane < nw) warp_tot[lane] = t;
-    if (lane == nw - 1 && total) *total = t;
-  }
-  __syncthreads();
-  int res = x - v + (warp ? warp_tot[warp - 1] : 0);
-  __syncthreads();
-  return res;
-}
 
 // descending bitonic sort of n (power of two) keys
 __device__ void bitonic_desc(unsigned long long* a, int n) {
@@ -542,7 +495,7 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   __shared__ uint32_t hist[SEL_BINS];      // level histograms (own partial, then cluster totals)
   __shared__ uint32_t tot[slice];          // cluster totals of this CTA's slice of bins
   __shared__ int warp_tot[32];
-  __shared__ int s_sum, s_bin, s_ncand, s_over, s_nsel, s_off, s_total_c, s_any_over;
+  __shared__ int s_bin, s_ncand, s_over, s_nsel, s_off, s_total_c, s_any_over;
   __shared__ int s_cnt[CL];
   __shared__ long long s_above;
   __shared__ unsigned long long s_tau;
@@ -743,16 +696,9 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   } else {
     // ---- slow path (crowded bucket): refine the key range level by level ----
     unsigned long long base, width;
-    if (fp_keys) { base = (unsigned long long)B0 << 41; width = 1ull << 41; }
-    else if (B0 < 64) { base = B0; width = 1; }
-    else {
-      int e = (B0 - 64) / 64 + 6, m = (B0 - 64) % 64;
-      base = (1ull << e) + ((unsigned long long)m << (e - 6));
-      width = 1ull << (e - 6);
-    }
+    bucket_range(B0, fp_keys, base, width);
     while (width > 1) {
-      const int lw = 63 - __clzll((long long)width);
-      const int shift = lw > 12 ? lw - 12 : 0;
+      const int shift = refine_shift(width);
       cluster_sync();     // peers finished reading tot[] of the previous level
       for (int b = tid; b < SEL_BINS; b += blockDim.x) hist[b] = 0;
       __syncthreads();
@@ -859,8 +805,17 @@ hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, con
 }
 
 hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                        int32_t* d_topk, cudaStream_t st, bool fp_keys) {
-  // 16 CTAs per token: each CTA's chunk is smaller and every pass shorter
+                        int32_t* d_topk, cudaStream_t st, bool fp_keys, bool wide_ok) {
+  // few query tokens: one wide group of co-resident CTAs per token, all SMs busy
+  const int sms = num_sms(), g_min = sel_wide_min_g(p->cfg.max_ctx);
+  if (wide_ok && n >= 1 && n <= p->d.sel_ws_tokens && n * g_min <= sms) {
+    int G = sms / n;
+    if (G > SW_MAX_G) G = SW_MAX_G;
+    const int g_want = (p->cfg.max_ctx + SW_TARGET - 1) / SW_TARGET;
+    if (G > g_want) G = g_want > g_min ? g_want : g_min;
+    return launch_select_wide(p, n, scores, ld, d_limit, d_topk, fp_keys, G, st);
+  }
+  // otherwise 16 CTAs per token: each CTA's chunk is smaller and every pass shorter
   return launch_select_cl<16>(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
 }
 

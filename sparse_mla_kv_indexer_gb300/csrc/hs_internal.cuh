@@ -55,6 +55,8 @@ struct Dev {
   int64_t* scores;      // [max_tokens, max_ctx]
   __half* o_part;       // [max_tokens, MAX_SPLITS, 512, 64] fp16 partial attention outputs
   float2* o_stats;      // [max_tokens, MAX_SPLITS, 64] per split and head: (max in log2 units, sum)
+  uint8_t* sel_ws;      // [sel_ws_tokens] SelWs: wide top-K selection scratch, zero between launches
+  int32_t sel_ws_tokens;
 };
 
 enum Counter { C_RESIDENT = 0, C_HITS = 1, C_MISSES = 2, C_H2D = 3, C_D2H = 4, C_N = 8 };
@@ -410,9 +412,10 @@ inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 // ---- host-side launch helpers (defined in hs_pool.cu) ----------------------------
 hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
                          const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, cudaStream_t st);
-// fp_keys: the scores are order-preserving keys of fp32 scores (FP8 indexer)
+// fp_keys: the scores are order-preserving keys of fp32 scores (FP8 indexer);
+// wide_ok: the pool's selection scratch may be used (few tokens: the wide kernel)
 hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                        int32_t* d_topk, cudaStream_t st, bool fp_keys = false);
+                        int32_t* d_topk, cudaStream_t st, bool fp_keys = false, bool wide_ok = true);
 hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* d_req,
                          const int32_t* d_topk, int32_t* d_row_ids, hs_plan_entry* d_plan,
                          cudaStream_t st);

@@ -12,7 +12,7 @@
 #include <cstring>
 #include <new>
 
-#include "hs_internal.cuh"
+#include "hs_select.cuh"
 
 using namespace hs;
 
@@ -260,6 +260,13 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   chk(dev_alloc(p, &D.scores, (size_t)c.max_tokens * c.max_ctx, 0));
   chk(dev_alloc(p, &D.o_part, (size_t)c.max_tokens * MAX_SPLITS * 512 * 64, 0));
   chk(dev_alloc(p, &D.o_stats, (size_t)c.max_tokens * MAX_SPLITS * 64, 0));
+  {
+    const int g_min = sel_wide_min_g(c.max_ctx);
+    int tok = num_sms() / g_min;
+    if (tok > c.max_tokens) tok = c.max_tokens;
+    D.sel_ws_tokens = tok;
+    chk(dev_alloc(p, &D.sel_ws, (size_t)(tok > 0 ? tok : 1) * sizeof(SelWs), 0));
+  }
   if (s == HS_OK) {
     if (cudaMemcpy(D.kv, d_kv_layers, sizeof(void*) * c.n_layers, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(D.idx, d_idx_layers, sizeof(void*) * n_groups, cudaMemcpyHostToDevice) != cudaSuccess ||

@@ -1,0 +1,117 @@
+// Pieces shared by the two top-K selection kernels (one cluster per query token,
+// and one wide group of CTAs per query token).
+//
+// Each score s of token index t is made unique and order-preserving as the key
+//   key = s * 2^21 + (2^21 - 1 - t)          (s >= 0, t < 2^21)
+// so the top K by (score desc, token asc) are exactly the K largest keys, and the
+// K-th largest key tau selects them with the single test key >= tau.
+#pragma once
+
+#include "hs_internal.cuh"
+
+namespace hs {
+
+constexpr int SEL_BINS = 4096;
+constexpr unsigned long long IDX_MASK = (1ull << 21) - 1;
+
+__device__ __forceinline__ unsigned long long sel_key(long long score, int t) {
+  return ((unsigned long long)score << 21) | (IDX_MASK - (unsigned long long)t);
+}
+__device__ __forceinline__ int sel_token(unsigned long long key) { return (int)(IDX_MASK - (key & IDX_MASK)); }
+
+// monotone level-0 bucket of a key: exact below 64, then 64 buckets per octave
+__device__ __forceinline__ int bucket1(unsigned long long v) {
+  if (v < 64) return (int)v;
+  int e = 63 - __clzll((long long)v);
+  int m = (int)((v >> (e - 6)) & 63);
+  return 64 + (e - 6) * 64 + m;
+}
+
+// Level-0 bucket of a key. Integer scores (exact int64) span many octaves: log
+// buckets. Order-preserving keys of fp32 scores lie in one octave of the key space:
+// their top 12 bits (sign, exponent, 3 mantissa bits) are 4,096 monotone buckets.
+__device__ __forceinline__ int bucket_of(unsigned long long k, bool fp_keys) {
+  return fp_keys ? (int)(k >> 41) : bucket1(k);
+}
+
+// Key range [base, base + width) of level-0 bucket b; consecutive buckets tile
+// the key space without gaps.
+__device__ __forceinline__ void bucket_range(int b, bool fp_keys, unsigned long long& base,
+                                             unsigned long long& width) {
+  if (fp_keys) {
+    base = (unsigned long long)b << 41;
+    width = 1ull << 41;
+  } else if (b < 64) {
+    base = (unsigned long long)b;
+    width = 1;
+  } else {
+    const int e = (b - 64) / 64 + 6, m = (b - 64) % 64;
+    base = (1ull << e) + ((unsigned long long)m << (e - 6));
+    width = 1ull << (e - 6);
+  }
+}
+
+// Shift that splits a key range of `width` (a power of two) into at most 4,096 bins.
+__device__ __forceinline__ int refine_shift(unsigned long long width) {
+  const int lw = 63 - __clzll((long long)width);
+  return lw > 12 ? lw - 12 : 0;
+}
+
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < nw) warp_tot[lane] = t;
+    if (lane == nw - 1 && total) *total = t;
+  }
+  __syncthreads();
+  int res = x - v + (warp ? warp_tot[warp - 1] : 0);
+  __syncthreads();
+  return res;
+}
+
+// ---- wide selection: one group of G co-resident CTAs per query token ----------------
+constexpr int SW_THREADS = 512;
+constexpr int SW_CHUNK = 12288;       // keys per CTA, held in shared memory
+constexpr int SW_CAND = 4096;         // keys of the final range every CTA loads to find tau
+constexpr int SW_LEVELS = 6;          // histogram levels (4,096 bins each) down to single keys
+constexpr int SW_MAX_G = 256;         // CTAs per query token
+constexpr int SW_MIN_G = 8;
+constexpr int SW_TARGET = 2048;       // keys per CTA the launch aims for
+constexpr int SW_SMEM = SW_CHUNK * 8 + SW_CAND * 8 + 16;
+
+// Per query token, in global memory; all zero between launches (the last CTA of a
+// launch clears what it used).
+struct SelWs {
+  uint32_t bar;                       // grid-barrier arrivals
+  uint32_t exit;                      // CTAs finished
+  uint32_t ncand;                     // keys of the final range appended to cand
+  uint32_t pad;
+  uint32_t above[SW_MAX_G];           // per CTA: its keys above the final range
+  uint32_t hist[SW_LEVELS][SEL_BINS]; // per level: sum of the CTAs' histograms
+  unsigned long long cand[SW_CAND];
+};
+
+// CTAs per query token the pool's selection scratch is sized for.
+inline int sel_wide_min_g(int max_ctx) {
+  const int g = (max_ctx + SW_CHUNK - 1) / SW_CHUNK;
+  return g > SW_MIN_G ? g : SW_MIN_G;
+}
+
+hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                             int32_t* d_topk, bool fp_keys, int G, cudaStream_t st);
+
+}  // namespace hs

@@ -1,0 +1,102 @@
+"""Top-K selection edge cases through hs_indexer_topk, against the oracle's full sort.
+
+Key caches are built so that the scores are crowded: every key equal (all scores
+tie, the K lowest token ids win), all scores zero, three distinct scores over
+262,144 tokens, and plain random keys. Each runs with 1 and 2 query tokens (the
+wide selection, one group of CTAs per token over the whole GPU), with 8 query
+tokens (the cluster selection) and through hs_indexer_topk_noalloc (the cluster
+selection, no pool scratch); ragged limits and a limit below K are included.
+The oracle's top-K (vLLM blog Part 1, "Sparsity when you need it"; ties to the
+lower token index) is a full sort of the exact int64 scores.
+"""
+import numpy as np
+import pytest
+
+from oracle import indexer as OI
+
+pytestmark = pytest.mark.gpu
+
+CTX = 262144
+K = 2048
+HI = 16
+
+
+def _torch():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+def _keys(kind, rng):
+    if kind == "equal":
+        k = rng.integers(1, 40, size=128, dtype=np.int64)
+        return np.broadcast_to(k, (CTX, 128)).astype(np.int8)
+    if kind == "three":
+        base = rng.integers(-60, 60, size=(3, 128), dtype=np.int64)
+        return base[rng.integers(0, 3, size=CTX)].astype(np.int8)
+    return np.clip(np.rint(rng.normal(0, 32, size=(CTX, 128))), -127, 127).astype(np.int8)
+
+
+def _queries(kind, n_tok, rng):
+    if kind == "zero":
+        q = np.zeros((n_tok, HI, 128), np.int8)
+    else:
+        q = np.clip(np.rint(rng.normal(0, 32, size=(n_tok, HI, 128))), -127, 127).astype(np.int8)
+        if kind == "equal":
+            q = np.abs(q)           # positive dot products with the all-positive key
+    w = rng.integers(1, 17, size=(n_tok, HI)).astype(np.int8)
+    return q, w
+
+
+# (request of each token, limit of each token)
+BATCHES = {
+    1: ([0], [CTX]),
+    2: ([0, 1], [CTX - 1000, 131073]),
+    8: ([0, 0, 0, 0, 1, 1, 1, 1], [200001, 200002, 200003, 200004, 1000, 1001, K + 1, CTX]),
+}
+
+
+@pytest.mark.parametrize("kind", ["equal", "zero", "three", "random"])
+def test_selection_matches_full_sort(kind):
+    torch = _torch()
+    from sparse_mla_kv_indexer_gb300 import hisparse as H
+    rng = np.random.default_rng({"equal": 1, "zero": 2, "three": 3, "random": 4}[kind])
+    keys = _keys("equal" if kind == "zero" else kind, rng)
+    pages = CTX // 64
+    pc = H.PoolConfig(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=HI, n_heads=16, topk=K,
+                      n_layers=1, layers_per_indexer=1, num_pages=4, num_idx_pages=pages, max_requests=2,
+                      max_ctx=CTX, max_q_per_req=4, hot_rows=4096, max_tokens=8, idx_format=H.IDX_INT8,
+                      host_pages=1)
+    kv = [torch.zeros(4 * 64 * 656, dtype=torch.uint8, device="cuda")]
+    ix = [torch.from_numpy(np.ascontiguousarray(keys).reshape(-1)).to("cuda")]
+    host = torch.zeros(64 * 656, dtype=torch.uint8, pin_memory=True)
+    pool = H.Pool(pc, kv, ix, host)
+    try:
+        for r in range(2):
+            pool.set_pages(r, 0, idx_pages=list(range(pages)))
+        for n_tok, (reqs, limits) in BATCHES.items():
+            q, w = _queries(kind, n_tok, rng)
+            want = np.stack([OI.topk(OI.scores(q[i], w[i], keys[:limits[i]]), K) for i in range(n_tok)])
+            d_req = torch.tensor(reqs, dtype=torch.int32, device="cuda")
+            d_lim = torch.tensor(limits, dtype=torch.int32, device="cuda")
+            d_q = torch.from_numpy(q.reshape(n_tok, -1)).to("cuda")
+            d_w = torch.from_numpy(w).to("cuda")
+            for entry in ("regular", "noalloc"):
+                out = torch.full((n_tok, K), -7, dtype=torch.int32, device="cuda")
+                for _ in range(2):   # the wide selection clears its scratch for the next call
+                    if entry == "regular":
+                        pool.indexer_topk(0, d_req, d_lim, d_q, d_w, out)
+                    else:
+                        pool.indexer_topk_noalloc(0, d_req, d_lim, d_q, d_w, out)
+                    torch.cuda.synchronize()
+                    assert pool.get_error() == 0, (kind, n_tok, entry)
+                    got = out.cpu().numpy()
+                    for i in range(n_tok):
+                        assert np.array_equal(got[i], want[i]), (kind, n_tok, entry, i)
+            if kind == "equal":
+                for i in range(n_tok):   # all scores tie: the K lowest token ids
+                    m = min(K, limits[i])
+                    assert np.array_equal(want[i][:m], np.arange(m)), i
+    finally:
+        pool.close()
