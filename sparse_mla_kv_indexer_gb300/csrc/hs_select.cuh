@@ -93,13 +93,15 @@ constexpr int SW_MIN_G = 8;
 constexpr int SW_TARGET = 2048;       // keys per CTA the launch aims for
 constexpr int SW_SMEM = SW_CHUNK * 8 + SW_CAND * 8 + 16;
 
-// Per query token, in global memory; all zero between launches (the last CTA of a
-// launch clears what it used).
+// Per query token, in global memory. The arrival counter only grows; `base` is
+// its value when a launch starts (the previous launch stores it after its last
+// barrier). The histogram sums and ncand are zero between launches: each launch
+// clears what it used after its last barrier.
 struct SelWs {
-  uint32_t bar;                       // grid-barrier arrivals
-  uint32_t exit;                      // CTAs finished
+  unsigned long long bar;             // grid-barrier arrivals, all launches
+  unsigned long long base;            // bar at the start of the next launch
   uint32_t ncand;                     // keys of the final range appended to cand
-  uint32_t pad;
+  uint32_t pad[3];
   uint32_t above[SW_MAX_G];           // per CTA: its keys above the final range
   uint32_t hist[SW_LEVELS][SEL_BINS]; // per level: sum of the CTAs' histograms
   unsigned long long cand[SW_CAND];

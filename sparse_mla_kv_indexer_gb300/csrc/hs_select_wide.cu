@@ -18,7 +18,7 @@
 //    of their own keys lie above it. After one more barrier every CTA finds tau
 //    (the K-th largest key) in the list by itself, adds the counts of the CTAs
 //    before it to get its output offset, and writes its selected tokens in order.
-//  * The last CTA to finish clears the sums and counters for the next launch.
+//  * After the last barrier each CTA clears a share of the sums for the next launch.
 // Its successor may start launching only once every CTA is resident (after the
 // first barrier), so a dependent kernel cannot take the SM a CTA still waits for.
 #include "hs_select.cuh"
@@ -27,20 +27,19 @@ namespace hs {
 
 namespace {
 
-// Grid barrier of the G CTAs of one query token. After WAIT_NS the status
-// records HS_ERR_TIMEOUT and false is returned to every thread of the CTA.
-__device__ bool sw_barrier(uint32_t* ctr, uint32_t target, int32_t* status, int* s_ok) {
+// Grid barrier of the G CTAs of one query token: wait until the arrival counter
+// reaches `target`. After WAIT_NS the status records HS_ERR_TIMEOUT and false is
+// returned to every thread of the CTA.
+__device__ bool sw_barrier(unsigned long long* ctr, unsigned long long target, int32_t* status, int* s_ok) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
     int ok = 1;
     uint64_t t0 = 0;
     for (uint32_t it = 1;; ++it) {
-      uint32_t v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
       if (v >= target) break;
-      __nanosleep(32);
       if ((it & 63u) == 0) {
         const uint64_t now = globaltimer();
         if (t0 == 0) {
@@ -52,7 +51,6 @@ __device__ bool sw_barrier(uint32_t* ctr, uint32_t target, int32_t* status, int*
         }
       }
     }
-    __threadfence();
     *s_ok = ok;
   }
   __syncthreads();
@@ -65,15 +63,15 @@ __device__ bool sw_barrier(uint32_t* ctr, uint32_t target, int32_t* status, int*
 template <bool GLOBAL>
 __device__ void sw_find(const uint32_t* h, int need, int* warp_tot, int* s_bin, long long* s_above) {
   constexpr int PER = SEL_BINS / SW_THREADS;
+  static_assert(PER == 8, "two 16-byte loads per thread");
   const int tid = threadIdx.x;
-  uint32_t t[PER];
+  // thread tid holds bins 4095 - 8 tid down to 4088 - 8 tid: t[k] = bin 4095 - 8 tid - k
+  const uint4* hv = reinterpret_cast<const uint4*>(h + SEL_BINS - PER * (tid + 1));
+  const uint4 lo4 = GLOBAL ? __ldcg(hv) : hv[0], hi4 = GLOBAL ? __ldcg(hv + 1) : hv[1];
+  const uint32_t t[PER] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
   int local = 0;
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int b = SEL_BINS - 1 - (tid * PER + k);
-    t[k] = GLOBAL ? __ldcg(h + b) : h[b];
-    local += (int)t[k];
-  }
+  for (int k = 0; k < PER; ++k) local += (int)t[k];
   if (tid == 0) {
     *s_bin = 0;
     *s_above = 0;
@@ -105,9 +103,9 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int K = D.topk;
   SelWs* W = reinterpret_cast<SelWs*>(D.sel_ws) + tok;
-  __shared__ uint32_t hist[SEL_BINS];
+  __shared__ __align__(16) uint32_t hist[SEL_BINS];
   __shared__ int warp_tot[32];
-  __shared__ int s_bin, s_ok, s_cnt, s_hi, s_pos, s_off, s_last;
+  __shared__ int s_bin, s_ok, s_cnt, s_hi, s_pos, s_off;
   __shared__ long long s_above;
   __shared__ unsigned long long s_tau;
   __shared__ __align__(8) uint64_t s_bar;
@@ -141,6 +139,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   }
   const long long* s = reinterpret_cast<const long long*>(scores) + (size_t)tok * ld;
   const int lo = min(n, g * per), cnt = min(n, lo + per) - lo;
+  const unsigned long long bar0 = __ldcg(&W->base);   // stored by the previous launch
 
   // ---- the chunk's scores by bulk copy; keys; level-0 histogram ----
   const int even = cnt & ~1;
@@ -167,8 +166,8 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   __syncthreads();
   for (int b = tid; b < SEL_BINS; b += SW_THREADS)
     if (hist[b]) atomicAdd(&W->hist[0][b], hist[b]);
-  uint32_t nbar = 1;
-  if (!sw_barrier(&W->bar, nbar * G, D.status, &s_ok)) return;
+  unsigned long long nbar = 1;
+  if (!sw_barrier(&W->bar, bar0 + nbar * G, D.status, &s_ok)) return;
   griddep_launch();   // every CTA of the token is resident
 
   // ---- narrow the range holding the K-th largest key, level by level ----
@@ -193,7 +192,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     __syncthreads();
     for (int b = tid; b < SEL_BINS; b += SW_THREADS)
       if (hist[b]) atomicAdd(&W->hist[level][b], hist[b]);
-    if (!sw_barrier(&W->bar, ++nbar * G, D.status, &s_ok)) return;
+    if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
     sw_find<true>(W->hist[level], need, warp_tot, &s_bin, &s_above);
     n_range = (int)__ldcg(&W->hist[level][s_bin]);
     base += (unsigned long long)s_bin << shift;
@@ -232,7 +231,18 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
       if (at < SW_CAND) W->cand[at] = k;
     }
   }
-  if (!sw_barrier(&W->bar, ++nbar * G, D.status, &s_ok)) return;
+  if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
+  // every CTA has read the sums and appended its keys: clear a share of what
+  // this launch used, and record where the next launch's barriers start
+  {
+    const int words = level * SEL_BINS, share = (words + G - 1) / G;
+    uint32_t* sums = &W->hist[0][0];
+    for (int j = g * share + tid; j < min(words, (g + 1) * share); j += SW_THREADS) sums[j] = 0;
+    if (g == 0 && tid == 0) {
+      W->ncand = 0;
+      W->base = bar0 + nbar * G;
+    }
+  }
 
   // ---- tau: the need-th largest key of the list, found alike by every CTA ----
   const int nc = min(n_range, SW_CAND);
@@ -295,24 +305,6 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
       else set_status(D.status, HS_ERR_BAD_ID);
     }
     wbase += __popc(m);
-  }
-
-  // ---- the last CTA of the token clears the scratch it used ----
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(&W->exit, 1u) == (uint32_t)G - 1;
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    for (int l = 0; l < level; ++l)
-      for (int b = tid; b < SEL_BINS; b += SW_THREADS) W->hist[l][b] = 0;
-    if (tid == 0) {
-      W->ncand = 0;
-      W->bar = 0;
-      W->exit = 0;
-    }
   }
 }
 
