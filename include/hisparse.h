@@ -240,7 +240,15 @@ hs_status hs_replay_topk(hs_pool* pool, int32_t group, int32_t n_tokens, const i
  *  d_q [n, H, 576] bf16, 16-byte aligned; d_row_ids [n, K] (-1 skipped);
  *  d_out [n, H, 512] bf16, 16-byte aligned; d_lse nullable [n, H] fp32.
  *  Per-group FP8 scales must be below 256 (HS_ERR_INVALID for misaligned
- *  pointers or out-of-range arguments). */
+ *  pointers or out-of-range arguments).
+ *  Layers of one selection: when the previous launch of this pool was
+ *  hs_sparse_mla_decode with the same d_row_ids on the same stream, the kernel
+ *  reads the row ids and gathers the rows while that kernel finishes
+ *  (programmatic dependent launch) and reads d_q only after it completes.
+ *  Between two such calls, d_row_ids and the KV rows may change only through
+ *  stream work that is not a programmatic-dependent kernel (an ordinary kernel
+ *  launch, a copy or a memset). Any other call of this library on the pool ends
+ *  the pairing. */
 hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, int32_t n_tokens,
                                const uint16_t* d_q, const int32_t* d_row_ids, float sm_scale,
                                uint16_t* d_out, float* d_lse, hs_stream_t stream);

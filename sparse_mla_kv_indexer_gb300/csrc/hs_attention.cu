@@ -124,7 +124,7 @@ __device__ __forceinline__ uint32_t cluster_size() {
 template <int HPC>
 __global__ void __launch_bounds__(AT_THREADS, 1)
 attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t* __restrict__ row_ids,
-                 float scale_log2, uint16_t* __restrict__ out, float* __restrict__ lse_out) {
+                 float scale_log2, uint16_t* __restrict__ out, float* __restrict__ lse_out, int settled) {
   using PL = AtPlan<HPC>;
   constexpr int HW = PL::HW;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -171,11 +171,17 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     fence_mbar_init();
   }
   if constexpr (PL::DSM) cluster_arrive_relaxed();   // this CTA has started; its barriers are initialised
-  griddep_wait();
-  griddep_launch();
+  // Settled: the row ids and the rows were written before the kernel this one
+  // follows (an earlier layer of the same selection), so they are read while that
+  // kernel finishes, through L2; q may come from that kernel and waits for it.
+  if (!settled) {
+    griddep_wait();
+    griddep_launch();
+  }
   if (tid < ATTN_ROWS) {
     const int k = (int)split * ATTN_ROWS + tid;
-    int id = k < K ? row_ids[(size_t)tok * K + k] : -1;
+    const int32_t* src = row_ids + (size_t)tok * K + k;
+    int id = k < K ? (settled ? __ldcg(src) : *src) : -1;
     if (id >= max_row) { set_status(D.status, HS_ERR_BAD_ID); id = -1; }
     ids[tid] = id;
   }
@@ -183,11 +189,24 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   const uint16_t* qt = q + ((size_t)tok * H + (size_t)hgrp * HPC) * QK;
   constexpr int QPT = (HPC * 72 + AT_THREADS - 1) / AT_THREADS;
   uint4 qv[QPT];
+  auto load_q = [&]() {
 #pragma unroll
-  for (int k = 0; k < QPT; ++k) {
-    const int c = tid + k * AT_THREADS;
-    qv[k] = c < HPC * 72 ? __ldg(reinterpret_cast<const uint4*>(qt) + c) : make_uint4(0, 0, 0, 0);
-  }
+    for (int k = 0; k < QPT; ++k) {
+      const int c = tid + k * AT_THREADS;
+      qv[k] = c < HPC * 72 ? __ldg(reinterpret_cast<const uint4*>(qt) + c) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto place_q = [&]() {
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int c = tid + k * AT_THREADS;
+      if (c < HPC * 72) {
+        const int h = c / 72, ch = c - h * 72;
+        *reinterpret_cast<uint4*>(Qs + (ch >> 3) * PL::Q_COL + sw128_chunk(h, ch & 7)) = qv[k];
+      }
+    }
+  };
+  if (!settled) load_q();
   __syncthreads();   // ids ready
   // ---- all row chunks in flight at once: chunk c = row * 41 + part ----
   uint4 rc[AT_CPT];
@@ -198,17 +217,13 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     if (c < AT_CHUNKS) {
       const int r = c / ROW_CHUNKS, part = c - r * ROW_CHUNKS;
       const int id = ids[r];
-      if (id >= 0) rc[k] = __ldg(reinterpret_cast<const uint4*>(kv + (size_t)id * ROW) + part);
+      if (id >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(kv + (size_t)id * ROW) + part;
+        rc[k] = settled ? __ldcg(src) : __ldg(src);
+      }
     }
   }
-#pragma unroll
-  for (int k = 0; k < QPT; ++k) {
-    const int c = tid + k * AT_THREADS;
-    if (c < HPC * 72) {
-      const int h = c / 72, ch = c - h * 72;
-      *reinterpret_cast<uint4*>(Qs + (ch >> 3) * PL::Q_COL + sw128_chunk(h, ch & 7)) = qv[k];
-    }
-  }
+  if (!settled) place_q();
 #pragma unroll
   for (int k = 0; k < AT_CPT; ++k) {
     const int c = tid + k * AT_THREADS;
@@ -228,6 +243,12 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
         *reinterpret_cast<uint4*>(KV + 8 * AT_KV_COL + sw128_chunk(r, part - 33)) = v;
       }
     }
+  }
+  if (settled) {
+    griddep_wait();
+    griddep_launch();
+    load_q();
+    place_q();
   }
   fence_proxy_async();
   tc_fence_before();
@@ -565,7 +586,7 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
 template <int HPC>
 static hs_status launch_attention_hpc(hs_pool* p, int layer, int n, int n_splits, const uint16_t* d_q,
                                       const int32_t* d_rows, float scale_log2, uint16_t* d_out, float* d_lse,
-                                      cudaStream_t st) {
+                                      bool settled, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(attention_kernel<HPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -576,11 +597,11 @@ static hs_status launch_attention_hpc(hs_pool* p, int layer, int n, int n_splits
   }
   const int n_hgrp = p->cfg.n_heads / HPC;
   return launch_pdl(attention_kernel<HPC>, dim3(n_splits, n * n_hgrp, 1), dim3(AT_THREADS, 1, 1), AtPlan<HPC>::SMEM,
-                    st, n_splits, p->d, layer, d_q, d_rows, scale_log2, d_out, d_lse);
+                    st, n_splits, p->d, layer, d_q, d_rows, scale_log2, d_out, d_lse, settled ? 1 : 0);
 }
 
 hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows, float sm_scale,
-                           uint16_t* d_out, float* d_lse, cudaStream_t st) {
+                           uint16_t* d_out, float* d_lse, bool settled, cudaStream_t st) {
   const int n_splits = (p->cfg.topk + ATTN_ROWS - 1) / ATTN_ROWS;
   const int H = p->cfg.n_heads;
   // fewer heads per CTA while the head groups still fit on the SMs side by side
@@ -589,9 +610,9 @@ hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, co
   const int slice = ((512 + n_splits - 1) / n_splits + 7) & ~7;
   if (hpc == 32 && n_splits * slice > AtPlan<32>::RECV_DIMS) hpc = 16;   // receive buffer bound
   const float sl = sm_scale * LOG2E;
-  if (hpc == 16) return launch_attention_hpc<16>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
-  if (hpc == 32) return launch_attention_hpc<32>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
-  return launch_attention_hpc<64>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, st);
+  if (hpc == 16) return launch_attention_hpc<16>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, settled, st);
+  if (hpc == 32) return launch_attention_hpc<32>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, settled, st);
+  return launch_attention_hpc<64>(p, layer, n, n_splits, d_q, d_rows, sl, d_out, d_lse, settled, st);
 }
 
 }  // namespace hs

@@ -70,6 +70,11 @@ struct hs_pool {
   std::vector<int32_t> n_hot_host;   // leased pages per (req, group), mirrored on the host
   std::vector<void*> allocations;
   std::vector<CUtensorMap> idx_tmaps;   // HS_IDX_FP8: one per indexer layer, 128-byte swizzled key pages
+  // The last hot-path launch of this pool was hs_sparse_mla_decode over settled_rows
+  // on settled_stream (null: it was something else). A decode that follows it with
+  // the same rows on the same stream may read them before that kernel completes.
+  const void* settled_rows = nullptr;
+  void* settled_stream = nullptr;
 };
 
 namespace hs {
@@ -423,8 +428,10 @@ hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, co
                              const uint8_t* d_q, const float* d_w, int64_t* d_keys, float* d_scores, cudaStream_t st);
 hs_status launch_replay(hs_pool* p, int group, int n, const int32_t* d_req, const int32_t* d_topk,
                         int32_t* d_row_ids, cudaStream_t st);
+// settled: d_rows and the rows it names were written before the previous kernel of
+// the stream, which is a decode of the same rows (see hs_pool::settled_rows)
 hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows,
-                           float sm_scale, uint16_t* d_out, float* d_lse, cudaStream_t st);
+                           float sm_scale, uint16_t* d_out, float* d_lse, bool settled, cudaStream_t st);
 int num_sms();
 
 }  // namespace hs

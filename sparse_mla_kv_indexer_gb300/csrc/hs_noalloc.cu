@@ -54,6 +54,7 @@ extern "C" hs_status hs_indexer_topk_noalloc(hs_pool* p, int32_t index_layer, in
   if (n == 0) return HS_OK;
   if (!d_req || !d_limit || !d_q || !d_w || !d_topk || (reinterpret_cast<uintptr_t>(d_q) & 15)) return HS_ERR_INVALID;
   if (p->d.idx_fmt != HS_IDX_INT8) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if ((long long)n * p->cfg.max_ctx > kMaxScores) return HS_ERR_SCRATCH_LIMIT;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;

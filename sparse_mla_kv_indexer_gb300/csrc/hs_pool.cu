@@ -296,6 +296,7 @@ hs_status hs_request_set_pages(hs_pool* p, int32_t req, int32_t first_page, int3
   if (!p || req < 0 || req >= p->cfg.max_requests || first_page < 0 || n < 0 ||
       (long long)first_page + n > p->d.max_pages)
     return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t off = (size_t)req * p->d.max_pages + first_page;
@@ -318,6 +319,7 @@ hs_status hs_hot_lease(hs_pool* p, int32_t req, int32_t group, int32_t n, const 
   if (!p || req < 0 || req >= p->cfg.max_requests || group < 0 || group >= p->d.n_groups || n < 0 ||
       (n > 0 && !h_pool_pages))
     return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   const size_t rg = (size_t)req * p->d.n_groups + group;
   const int cur = p->n_hot_host[rg];
   if (cur + n > p->d.hot_pages_max) return HS_ERR_INVALID;
@@ -335,6 +337,7 @@ hs_status hs_hot_lease(hs_pool* p, int32_t req, int32_t group, int32_t n, const 
 
 hs_status hs_hot_release(hs_pool* p, int32_t req, hs_stream_t stream) {
   if (!p || req < 0 || req >= p->cfg.max_requests) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   clear_hot_kernel<<<launch_blocks(p->cfg.max_ctx, 256), 256, 0, st>>>(p->d, req);
   HS_CUDA_TRY(cudaGetLastError());
@@ -345,6 +348,7 @@ hs_status hs_hot_release(hs_pool* p, int32_t req, hs_stream_t stream) {
 hs_status hs_append_rows(hs_pool* p, int32_t n, const int32_t* d_req, const int32_t* d_pos, const uint8_t* d_kv_rows,
                          const int8_t* d_idx_keys, hs_stream_t stream) {
   if (!p || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
   if (!d_req || !d_pos || !d_kv_rows || !d_idx_keys || !aligned16(d_kv_rows) || !aligned16(d_idx_keys))
     return HS_ERR_INVALID;
@@ -357,6 +361,7 @@ hs_status hs_indexer_topk(hs_pool* p, int32_t index_layer, int32_t n, const int3
                           const int8_t* d_q, const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,
                           hs_stream_t stream) {
   if (!p || index_layer < 0 || index_layer >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
   if (!d_req || !d_limit || !d_q || !d_w || !d_topk || !aligned16(d_q)) return HS_ERR_INVALID;
   if (d_scores && !aligned16(d_scores)) return HS_ERR_INVALID;
@@ -372,6 +377,7 @@ hs_status hs_indexer_topk_fp8(hs_pool* p, int32_t index_layer, int32_t n, const 
                               const int32_t* d_limit, const uint8_t* d_q, const float* d_w, int32_t* d_topk,
                               float* d_scores, hs_stream_t stream) {
   if (!p || index_layer < 0 || index_layer >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
   if (p->d.idx_fmt != HS_IDX_FP8) return HS_ERR_INVALID;
   if (!d_req || !d_limit || !d_q || !d_w || !d_topk || !aligned16(d_q) || (reinterpret_cast<uintptr_t>(d_w) & 3))
@@ -386,6 +392,7 @@ hs_status hs_indexer_topk_fp8(hs_pool* p, int32_t index_layer, int32_t n, const 
 hs_status hs_resolve_topk(hs_pool* p, int32_t group, int32_t step, int32_t n, const int32_t* d_req,
                           const int32_t* d_topk, int32_t* d_row_ids, hs_plan_entry* d_plan, hs_stream_t stream) {
   if (!p || group < 0 || group >= p->d.n_groups || step < 0 || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
   if (!d_req || !d_topk || !d_row_ids) return HS_ERR_INVALID;
   return launch_resolve(p, group, step, n, d_req, d_topk, d_row_ids, d_plan, reinterpret_cast<cudaStream_t>(stream));
@@ -394,6 +401,7 @@ hs_status hs_resolve_topk(hs_pool* p, int32_t group, int32_t step, int32_t n, co
 hs_status hs_replay_topk(hs_pool* p, int32_t group, int32_t n, const int32_t* d_req, const int32_t* d_topk,
                          int32_t* d_row_ids, hs_stream_t stream) {
   if (!p || group < 0 || group >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
   if (!d_req || !d_topk || !d_row_ids) return HS_ERR_INVALID;
   return launch_replay(p, group, n, d_req, d_topk, d_row_ids, reinterpret_cast<cudaStream_t>(stream));
@@ -404,12 +412,20 @@ hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, int32_t n, const uint1
   if (!p || layer < 0 || layer >= p->cfg.n_layers || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   if (n == 0) return HS_OK;
   if (!d_q || !d_row_ids || !d_out || !aligned16(d_q) || !aligned16(d_out)) return HS_ERR_INVALID;
-  return launch_attention(p, layer, n, d_q, d_row_ids, sm_scale, d_out, d_lse, reinterpret_cast<cudaStream_t>(stream));
+  // the previous launch of this pool was a decode over the same rows on this stream:
+  // the row ids and rows are final before that kernel started
+  const bool settled = p->settled_rows == d_row_ids && p->settled_stream == stream;
+  const hs_status s = launch_attention(p, layer, n, d_q, d_row_ids, sm_scale, d_out, d_lse, settled,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  p->settled_rows = s == HS_OK ? d_row_ids : nullptr;
+  p->settled_stream = stream;
+  return s;
 }
 
 hs_status hs_offload_pages(hs_pool* p, int32_t n, const int32_t* d_pool_pages, const int64_t* d_host_pages,
                            hs_stream_t stream) {
   if (!p || n < 0) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
   if (!d_pool_pages || !d_host_pages) return HS_ERR_INVALID;
   const long long work = (long long)n * p->d.n_layers * (PAGE * ROW / 16);
