@@ -37,12 +37,16 @@ namespace hs {
 // Scoring kernel
 // ----------------------------------------------------------------------------------
 // Warp roles (448 threads):
-//   warps 0-3   epilogue: TMEM accumulator -> ReLU, head weights, int64 scores
-//   warps 4-11  convert: raw int8 key tile -> fp16 A tile; queries -> fp16 B operand
+//   warps 0-7   epilogue, two warpgroups on alternate tiles (one tile's TMEM reads
+//               and dependent arithmetic overlap the other's): TMEM accumulator ->
+//               ReLU, head weights, int64 scores
+//   warps 8-11  convert: raw int8 key tile -> fp16 A tile; queries -> fp16 B operand
 //   warp 12     producer: bulk copies of key pages into the stage ring
 //   warp 13     MMA issuer: tcgen05.mma into one of the TMEM accumulators
 constexpr int IX_THREADS = 448;
-constexpr int IX_CONV = 256;                           // converter threads
+constexpr int IX_EPI_GROUPS = 2;
+constexpr int IX_CONV_WARP0 = 8;
+constexpr int IX_CONV = 128;                           // converter threads
 constexpr int IX_PRODUCER_WARP = 12, IX_MMA_WARP = 13;
 constexpr int IX_MAX_A = 4;                            // fp16 A tiles in flight
 constexpr int IX_MAX_STAGES = 12;
@@ -67,7 +71,7 @@ struct IxLayout {
 IxLayout ix_layout(int n_max_rows, int max_tokens) {
   IxLayout L;
   L.b_col = n_max_rows * 128;
-  const int tail = 512 + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 64 + 1024;
+  const int tail = 512 + max_tokens * 16 + IX_EPI_GROUPS * (4 * 64 * 4 + 64) + 2 * max_tokens * 4 + 1024;
   // as many A tiles as leave at least three key stages, then every remaining byte to the key ring
   for (L.n_a = IX_MAX_A; L.n_a > 2; --L.n_a)
     if ((IX_SMEM_BUDGET - L.n_a * IX_A - 2 * L.b_col - tail) / IX_RAW >= 3) break;
@@ -77,7 +81,7 @@ IxLayout ix_layout(int n_max_rows, int max_tokens) {
   L.stages = stages > IX_MAX_STAGES ? IX_MAX_STAGES : stages;
   L.off_bar = L.off_raw + L.stages * IX_RAW;
   L.off_seg = L.off_bar + 512;
-  L.smem = L.off_seg + max_tokens * 16 + 4 * 64 * 4 + 2 * max_tokens * 4 + 64 + 1024;
+  L.smem = L.off_seg + max_tokens * 16 + IX_EPI_GROUPS * (4 * 64 * 4 + 64) + 2 * max_tokens * 4 + 1024;
   L.acc_cols = 32;
   while (L.acc_cols < n_max_rows) L.acc_cols <<= 1;
   L.n_acc = IX_TMEM_COLS / L.acc_cols < IX_MAX_ACC ? IX_TMEM_COLS / L.acc_cols : IX_MAX_ACC;
@@ -115,6 +119,15 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Named barrier over n threads that also ORs a flag across them: every thread
+// leaves with the same answer.
+__device__ __forceinline__ int named_sync_or(int id, int n, int flag) {
+  int out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.s32 %0, 1, 0, q;\n}"
+      : "=r"(out) : "r"(flag), "r"(id), "r"(n) : "memory");
+  return out;
+}
 
 __global__ void __launch_bounds__(IX_THREADS, 1)
 indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, const int32_t* __restrict__ limit_of,
@@ -136,10 +149,10 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   int32_t* s_issued = s_nseg + 2;
   int32_t* s_consumed = s_nseg + 3;
   IxSeg* segs = reinterpret_cast<IxSeg*>(smem + L.off_seg);
-  int32_t* s_w = reinterpret_cast<int32_t*>(segs + D.max_tokens);                    // [4][64], epilogue-owned
-  int32_t* s_req = s_w + 4 * 64;                                                      // [n_tok]
-  int32_t* s_lim = s_req + D.max_tokens;                                              // [n_tok]
-  int32_t* s_wsum = s_lim + D.max_tokens;                                             // [4][4], epilogue-owned
+  int32_t* s_w = reinterpret_cast<int32_t*>(segs + D.max_tokens);   // [IX_EPI_GROUPS][4][64], per warpgroup
+  int32_t* s_req = s_w + IX_EPI_GROUPS * 4 * 64;                     // [n_tok]
+  int32_t* s_lim = s_req + D.max_tokens;                             // [n_tok]
+  int32_t* s_wsum = s_lim + D.max_tokens;                            // [IX_EPI_GROUPS][4][4], per warpgroup
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hi = D.n_idx_heads;
@@ -280,9 +293,9 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
         umma_commit(smem_u32(&t_full[tb]));
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= IX_CONV_WARP0) {
     // ------------------------------ converters ------------------------------
-    const int ct = tid - 128;
+    const int ct = tid - IX_CONV_WARP0 * 32;
     int cur_seg = -1;
     for (int i = 0; i < n_local; ++i) {
       const int item = item_of(i);
@@ -359,43 +372,51 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
     }
   } else {
     // ------------------------------ epilogue ------------------------------
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    // warpgroup grp takes tiles i = grp, grp + 2, ...; the accumulator count is even,
+    // so each accumulator stays with one warpgroup and its phase waits never alias
+    const int grp = warp >> 2, et = tid & 127;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    int32_t* sw = s_w + grp * 4 * 64;
+    int32_t* swsum = s_wsum + grp * 16;
     int cur_seg = -1;
-    for (int i = 0; i < n_local; ++i) {
+    for (int i = grp; i < n_local; i += IX_EPI_GROUPS) {
       const int item = item_of(i);
       const int sg = seg_of(item);
       const IxSeg S = segs[sg];
       const int tile = item - (sg ? segs[sg - 1].tile_end : 0);
-      const int key = tile * IX_TILE + warp * 32 + lane;
+      const int key = tile * IX_TILE + et;
       if (sg != cur_seg) {
-        named_sync(2, 128);
-        for (int c = tid; c < 4 * 64; c += 128) {
+        named_sync(2 + grp, 128);
+        for (int c = et; c < 4 * 64; c += 128) {
           const int j = c >> 6, h = c & 63;
           int w = 0;
           if (j < S.ntok && h < Hi) {
             w = wg[(size_t)(S.first + j) * Hi + h];
             if (w < 0) { set_status(D.status, HS_ERR_BAD_WEIGHT); w = 0; }
           }
-          s_w[c] = w;
+          sw[c] = w;
         }
-        named_sync(2, 128);
-        if (tid < 16) {   // sum of the weights of each 16-head group, per token
+        named_sync(2 + grp, 128);
+        if (et < 16) {   // sum of the weights of each 16-head group, per token
           int t = 0;
-          for (int k = 0; k < 16; ++k) t += s_w[(tid >> 2) * 64 + (tid & 3) * 16 + k];
-          s_wsum[tid] = t;
+          for (int k = 0; k < 16; ++k) t += sw[(et >> 2) * 64 + (et & 3) * 16 + k];
+          swsum[et] = t;
         }
-        named_sync(2, 128);
+        named_sync(2 + grp, 128);
         cur_seg = sg;
       }
       const int tb = i % L.n_acc;
-      if (!mbar_wait(smem_u32(&t_full[tb]), (i / L.n_acc) & 1, D.status)) { *s_dead = 1; break; }
+      // a failed wait is recorded and the tile run through without stores, so that the
+      // warpgroup's decision to stop is taken together at the barrier below
+      const int ok = mbar_wait(smem_u32(&t_full[tb]), (i / L.n_acc) & 1, D.status);
+      if (!ok) *s_dead = 1;
       tc_fence_after();
       // Exact integer epilogue without float->int conversions: every dot product
       // is an integer |d| <= 2^21 held exactly in fp32, so max(d, 0) + 2^23 has the
       // bit pattern 0x4B000000 + relu(d). With w <= 127, each w * relu(d) < 2^28 and
-      // 16 of them sum below 2^32: 16 heads accumulate bits * w in uint32 (mod 2^32)
-      // and the offset 0x4B000000 * sum(w) comes off once per group, which leaves the
-      // exact group sum; the groups add in 64 bits.
+      // 16 of them sum below 2^32: 16 heads accumulate bits * w in uint32 (mod 2^32,
+      // in four independent partial sums) and the offset 0x4B000000 * sum(w) comes
+      // off once per group, which leaves the exact group sum; the groups add in 64 bits.
       for (int j = 0; j < S.ntok; ++j) {
         const int lim = s_lim[S.first + j];
         const uint32_t col0 = lane_base + (uint32_t)(tb * L.acc_cols + j * Hi);
@@ -408,26 +429,25 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           if (q * 16 < Hi) {
-            uint32_t s32 = 0u - 0x4B000000u * (uint32_t)s_wsum[j * 4 + q];
+            uint32_t p[4] = {0u - 0x4B000000u * (uint32_t)swsum[j * 4 + q], 0u, 0u, 0u};
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-              const int4 w4 = *reinterpret_cast<const int4*>(s_w + j * 64 + q * 16 + k4 * 4);
+              const int4 w4 = *reinterpret_cast<const int4*>(sw + j * 64 + q * 16 + k4 * 4);
               const int w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const float d = fmaxf(__uint_as_float(r[q * 16 + k4 * 4 + k]), 0.f);
-                s32 += __float_as_uint(d + 8388608.f) * (uint32_t)w[k];
+                p[k] += __float_as_uint(d + 8388608.f) * (uint32_t)w[k];
               }
             }
-            acc += s32;
+            acc += (uint32_t)((p[0] + p[1]) + (p[2] + p[3]));
           }
         }
-        if (key < lim) scores[(size_t)(S.first + j) * ld + key] = (long long)acc;
+        if (ok && key < lim) scores[(size_t)(S.first + j) * ld + key] = (long long)acc;
       }
       tc_fence_before();
-      named_sync(2, 128);
-      if (tid == 0) mbar_arrive(smem_u32(&t_empty[tb]));
-      if (*(volatile int32_t*)s_dead) break;
+      if (named_sync_or(2 + grp, 128, *(volatile int32_t*)s_dead)) break;
+      if (et == 0) mbar_arrive(smem_u32(&t_empty[tb]));
     }
   }
   __syncthreads();
