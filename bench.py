@@ -105,7 +105,81 @@ def workload_config(name, steps_total, rank):
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
+class NvmlSampler:
+    """SM clock, its maximum, power and throttle reasons of this process's GPU, read
+    through NVML (read-only queries) every few milliseconds on a background thread,
+    so that a timed region of tens of milliseconds gets samples."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_slowdown"}
+
+    def __init__(self, cuda_device, period_s=0.005):
+        import ctypes
+        import threading
+        self.samples = []
+        self.ok = False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            rt = None
+            for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+                try:
+                    rt = ctypes.CDLL(name)
+                    break
+                except OSError:
+                    continue
+            bus = ctypes.create_string_buffer(32)
+            if rt is None or rt.cudaDeviceGetPCIBusId(bus, 32, ctypes.c_int(cuda_device)) != 0:
+                return
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.value, ctypes.byref(h)) != 0:
+                return
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._nv, self._h, self._reasons_fn, self._ct = nv, h, reasons_fn, ctypes
+        except Exception:
+            return
+        self.ok = True
+        self._stop = threading.Event()
+        self._period = period_s
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        ct, nv, h = self._ct, self._nv, self._h
+        sm, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(sm)) != 0:      # NVML_CLOCK_SM
+            return None
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ct.byref(mx))
+        nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+        self._reasons_fn(h, ct.byref(rs))
+        return sm.value, mx.value, mw.value / 1000.0, rs.value
+
+    def _run(self):
+        while not self._stop.is_set():
+            r = self._read()
+            if r:
+                self.samples.append(r)
+            self._stop.wait(self._period)
+
+    def stop(self):
+        if not self.ok:
+            return None
+        self._stop.set()
+        self._t.join(timeout=2)
+        if not self.samples:
+            return None
+        reasons = sorted({name for s in self.samples for bit, name in self.REASONS.items() if s[3] & bit})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": reasons,
+                "power_w": statistics.median(s[2] for s in self.samples),
+                "samples": len(self.samples), "source": "nvml"}
+
+
 class ClockSampler:
+    """nvidia-smi clocks line during the timed region; NVML samples (same source,
+    every 5 ms) are reported when available, since a short region may see no
+    nvidia-smi sample at its 200 ms period."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -114,6 +188,7 @@ class ClockSampler:
         self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
         self.gpu = gpu_index
         self.proc = None
+        self.nvml = NvmlSampler(gpu_index)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
@@ -123,6 +198,15 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        fast = self.nvml.stop()
+        smi = self._stop_smi()
+        if fast:
+            if smi:
+                fast["nvidia_smi_samples"] = smi["samples"]
+            return fast
+        return smi
+
+    def _stop_smi(self):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -145,7 +229,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": "nvidia-smi"}
 
 
 # ---------------------------------------------------------------------------
@@ -186,23 +270,34 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(kernel_file, name):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+def sources_sha256(files):
+    """sha256 over the call's kernel sources and the shared device header, in order."""
+    h = hashlib.sha256()
+    for f in list(files) + ["hs_internal.cuh"]:
+        h.update(open(os.path.join(ROOT, "sparse_mla_kv_indexer_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel_files, name, workload):
+    """DRAM bytes per launch of call `name` on `workload` from a committed ncu summary,
+    if taken on the current sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        ent = d[name]
-        src = open(os.path.join(ROOT, "sparse_mla_kv_indexer_gb300", "csrc", kernel_file), "rb").read()
-        if ent.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        ent = d[name + "@" + workload]
+        if ent.get("source_sha256") != sources_sha256(kernel_files):
             return None
         return ent.get("bytes_per_launch")
     except Exception:
         return None
 
 
-KERNEL_FILES = {"indexer_topk": "hs_indexer.cu", "sparse_mla_decode": "hs_attention.cu",
-                "resolve_topk": "hs_resolver.cu", "offload_pages": "hs_pool.cu", "append": "hs_pool.cu"}
+# the sources of each call's kernels (their sha256 keys the committed ncu traffic)
+KERNEL_FILES = {"indexer_topk": ["hs_indexer.cu", "hs_select.cuh", "hs_select_wide.cu"],
+                "indexer_topk_fp8": ["hs_indexer_fp8.cu", "hs_select.cuh", "hs_select_wide.cu"],
+                "sparse_mla_decode": ["hs_attention.cu"], "resolve_topk": ["hs_resolver.cu"],
+                "offload_pages": ["hs_pool.cu"], "append": ["hs_pool.cu"]}
 
 
 # ---------------------------------------------------------------------------
@@ -426,6 +521,7 @@ def main():
     peak, peak_kind = measured_peaks()
     dom_bytes = alg.get(dom, 0.0)
     achieved = dom_bytes / (avg_ms / 1000.0) / 1e9 if avg_ms > 0 else 0.0
+    tkey = dom + "_fp8" if dom == "indexer_topk" and cfg.idx_fp8 else dom   # key of the committed traffic
     step_bytes = alg["indexer_topk"] * cfg.n_groups + alg["sparse_mla_decode"] * cfg.n_layers
     roof_step_s = step_bytes / (peak * 1e9)
 
@@ -446,7 +542,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes,
-                     "traffic": ncu_traffic(KERNEL_FILES.get(dom, ""), dom)},
+                     "traffic": ncu_traffic(KERNEL_FILES.get(tkey, []), tkey, args.workload)},
         "step_roofline": {"algorithmic_hbm_bytes": step_bytes, "roofline_ms": roof_step_s * 1e3,
                           "frac": roof_step_s / (t_max / K)},
         "breakdown_ms_per_call": {k: v["ms"] for k, v in calls.items()},
