@@ -63,15 +63,16 @@ constexpr int IX_MAX_ACC = 8;
 struct IxLayout {
   int n_a;        // fp16 A tiles (3 or 4: conversion runs ahead of the MMA)
   int b_col;      // bytes per 64-dim atom column of the query operand (n_max rows x 128 B)
-  int off_b, off_raw, off_bar, off_seg, stages, smem;
+  int off_b, off_raw, off_bar, off_seg, off_hist, stages, smem;   // off_hist: 0 = no histogram
   int acc_cols;   // TMEM columns per accumulator (power of two >= n_max rows)
   int n_acc;      // accumulators in flight between the MMA warp and the epilogue
 };
 
-IxLayout ix_layout(int n_max_rows, int max_tokens) {
+IxLayout ix_layout(int n_max_rows, int max_tokens, bool hist) {
   IxLayout L;
   L.b_col = n_max_rows * 128;
-  const int tail = 512 + max_tokens * 16 + IX_EPI_GROUPS * (4 * 64 * 4 + 64) + 2 * max_tokens * 4 + 1024;
+  const int hist_bytes = hist ? SEL_BINS * 4 : 0;
+  const int tail = 512 + max_tokens * 16 + IX_EPI_GROUPS * (4 * 64 * 4 + 64) + 2 * max_tokens * 4 + hist_bytes + 1024;
   // as many A tiles as leave at least three key stages, then every remaining byte to the key ring
   for (L.n_a = IX_MAX_A; L.n_a > 2; --L.n_a)
     if ((IX_SMEM_BUDGET - L.n_a * IX_A - 2 * L.b_col - tail) / IX_RAW >= 3) break;
@@ -81,7 +82,8 @@ IxLayout ix_layout(int n_max_rows, int max_tokens) {
   L.stages = stages > IX_MAX_STAGES ? IX_MAX_STAGES : stages;
   L.off_bar = L.off_raw + L.stages * IX_RAW;
   L.off_seg = L.off_bar + 512;
-  L.smem = L.off_seg + max_tokens * 16 + IX_EPI_GROUPS * (4 * 64 * 4 + 64) + 2 * max_tokens * 4 + 1024;
+  L.off_hist = hist ? L.off_seg + max_tokens * 16 + IX_EPI_GROUPS * (4 * 64 * 4 + 64) + 2 * max_tokens * 4 : 0;
+  L.smem = L.off_seg + max_tokens * 16 + IX_EPI_GROUPS * (4 * 64 * 4 + 64) + 2 * max_tokens * 4 + hist_bytes + 1024;
   L.acc_cols = 32;
   while (L.acc_cols < n_max_rows) L.acc_cols <<= 1;
   L.n_acc = IX_TMEM_COLS / L.acc_cols < IX_MAX_ACC ? IX_TMEM_COLS / L.acc_cols : IX_MAX_ACC;
@@ -132,7 +134,7 @@ __device__ __forceinline__ int named_sync_or(int id, int n, int flag) {
 __global__ void __launch_bounds__(IX_THREADS, 1)
 indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, const int32_t* __restrict__ limit_of,
                const int8_t* __restrict__ qg, const int8_t* __restrict__ wg, int64_t* __restrict__ scores,
-               int ld, IxLayout L) {
+               int ld, IxLayout L, uint32_t* __restrict__ hist0) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NS = L.stages;
@@ -153,6 +155,9 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   int32_t* s_req = s_w + IX_EPI_GROUPS * 4 * 64;                     // [n_tok]
   int32_t* s_lim = s_req + D.max_tokens;                             // [n_tok]
   int32_t* s_wsum = s_lim + D.max_tokens;                            // [IX_EPI_GROUPS][4][4], per warpgroup
+  // hist0 (one query token, wide selection): the selection's level-0 histogram of
+  // this CTA's scores, added to the selection's global sums at the end
+  uint32_t* s_hist = hist0 ? reinterpret_cast<uint32_t*>(smem + L.off_hist) : nullptr;   // [SEL_BINS]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hi = D.n_idx_heads;
@@ -163,6 +168,8 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
     for (int b = 0; b < 2 * IX_MAX_STAGES + 2 * IX_MAX_A + 2 * IX_MAX_ACC; ++b) mbar_init(smem_u32(&bars[b]), 1);
     fence_mbar_init();
   }
+  if (s_hist)
+    for (int b = tid; b < SEL_BINS; b += IX_THREADS) s_hist[b] = 0;
   griddep_wait();
   griddep_launch();
   // ---- request segments of the batch (tokens of one request are contiguous) ----
@@ -443,11 +450,19 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
             acc += (uint32_t)((p[0] + p[1]) + (p[2] + p[3]));
           }
         }
-        if (ok && key < lim) scores[(size_t)(S.first + j) * ld + key] = (long long)acc;
+        if (ok && key < lim) {
+          scores[(size_t)(S.first + j) * ld + key] = (long long)acc;
+          if (s_hist) atomicAdd(&s_hist[bucket1(sel_key((long long)acc, key))], 1u);
+        }
       }
       tc_fence_before();
       if (named_sync_or(2 + grp, 128, *(volatile int32_t*)s_dead)) break;
       if (et == 0) mbar_arrive(smem_u32(&t_empty[tb]));
+    }
+    if (s_hist) {   // both warpgroups are done: this CTA's histogram to the global sums
+      named_sync(4, IX_EPI_GROUPS * 128);
+      for (int b = tid; b < SEL_BINS; b += IX_EPI_GROUPS * 128)
+        if (s_hist[b]) atomicAdd(&hist0[b], s_hist[b]);
     }
   }
   __syncthreads();
@@ -795,9 +810,10 @@ int num_sms() {
 }
 
 hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
-                         const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, cudaStream_t st) {
+                         const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, uint32_t* d_hist0,
+                         cudaStream_t st) {
   const int n_max = ((p->cfg.max_q_per_req * p->cfg.n_idx_heads) + 15) & ~15;
-  const IxLayout L = ix_layout(n_max, p->cfg.max_tokens);
+  const IxLayout L = ix_layout(n_max, p->cfg.max_tokens, d_hist0 != nullptr);
   if (L.stages < 2) return HS_ERR_INVALID;
   static int attr_smem = 0;
   if (attr_smem < L.smem) {
@@ -806,7 +822,7 @@ hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const 
     attr_smem = L.smem;
   }
   return launch_pdl(indexer_kernel, dim3(num_sms()), dim3(IX_THREADS), L.smem, st, 0, p->d, il, n, d_req, d_limit,
-                    d_q, d_w, d_scores, p->cfg.max_ctx, L);
+                    d_q, d_w, d_scores, p->cfg.max_ctx, L, d_hist0);
 }
 
 template <int CL>
@@ -824,17 +840,26 @@ hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, con
                     d_topk, fp_keys ? 1 : 0);
 }
 
-hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                        int32_t* d_topk, cudaStream_t st, bool fp_keys, bool wide_ok) {
+int select_wide_groups(hs_pool* p, int n, bool wide_ok) {
   // few query tokens: one wide group of co-resident CTAs per token, all SMs busy
   const int sms = num_sms(), g_min = sel_wide_min_g(p->cfg.max_ctx);
-  if (wide_ok && n >= 1 && n <= p->d.sel_ws_tokens && n * g_min <= sms) {
-    int G = sms / n;
-    if (G > SW_MAX_G) G = SW_MAX_G;
-    const int g_want = (p->cfg.max_ctx + SW_TARGET - 1) / SW_TARGET;
-    if (G > g_want) G = g_want > g_min ? g_want : g_min;
-    return launch_select_wide(p, n, scores, ld, d_limit, d_topk, fp_keys, G, st);
-  }
+  if (!wide_ok || n < 1 || n > p->d.sel_ws_tokens || n * g_min > sms) return 0;
+  int G = sms / n;
+  if (G > SW_MAX_G) G = SW_MAX_G;
+  const int g_want = (p->cfg.max_ctx + SW_TARGET - 1) / SW_TARGET;
+  if (G > g_want) G = g_want > g_min ? g_want : g_min;
+  return G;
+}
+
+uint32_t* select_hist0(hs_pool* p, int n, bool wide_ok) {
+  if (n != 1 || select_wide_groups(p, n, wide_ok) == 0) return nullptr;
+  return reinterpret_cast<SelWs*>(p->d.sel_ws)->hist[0];
+}
+
+hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                        int32_t* d_topk, cudaStream_t st, bool fp_keys, bool wide_ok, bool hist0_done) {
+  const int G = select_wide_groups(p, n, wide_ok);
+  if (G > 0) return launch_select_wide(p, n, scores, ld, d_limit, d_topk, fp_keys, G, hist0_done, st);
   // otherwise 16 CTAs per token: each CTA's chunk is smaller and every pass shorter
   return launch_select_cl<16>(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
 }

@@ -23,7 +23,7 @@
 //    form the fp32 score and store it as an order-preserving integer key for the
 //    top-K selection (and as fp32 when the caller asks), then release the
 //    accumulator and the stage.
-#include "hs_internal.cuh"
+#include "hs_select.cuh"
 
 namespace hs {
 
@@ -46,21 +46,24 @@ static_assert(F8_N_BARS * 8 + 32 <= 1024, "barriers and flags fit their region")
 
 struct F8Layout {
   int b_bytes;     // query operand [N][128] e4m3 (128-byte swizzled), 1 KB aligned
-  int off_stage, stages, off_sc, off_bar, off_seg, smem;
+  int off_stage, stages, off_sc, off_bar, off_seg, off_hist, smem;   // off_hist: 0 = no histogram
   int acc_cols, n_acc;
 };
 
-static F8Layout f8_layout(int n_max_rows, int max_tokens) {
+static F8Layout f8_layout(int n_max_rows, int max_tokens, bool hist) {
   F8Layout L;
   L.b_bytes = (n_max_rows * 128 + 1023) & ~1023;
   L.off_stage = L.b_bytes;
-  const int tail = F8_SC_BYTES + 1024 + max_tokens * 16 + F8_EPI_GROUPS * 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  const int hist_bytes = hist ? SEL_BINS * 4 : 0;
+  const int tail = F8_SC_BYTES + 1024 + max_tokens * 16 + F8_EPI_GROUPS * 4 * 64 * 4 + 2 * max_tokens * 4 +
+                   hist_bytes + 1024;
   const int st = (F8_BUDGET - L.off_stage - tail) / F8_STAGE;
   L.stages = st > F8_MAX_STAGES ? F8_MAX_STAGES : st;
   L.off_sc = L.off_stage + L.stages * F8_STAGE;
   L.off_bar = L.off_sc + F8_SC_BYTES;
   L.off_seg = L.off_bar + 1024;
-  L.smem = L.off_seg + max_tokens * 16 + F8_EPI_GROUPS * 4 * 64 * 4 + 2 * max_tokens * 4 + 1024;
+  L.off_hist = hist ? L.off_seg + max_tokens * 16 + F8_EPI_GROUPS * 4 * 64 * 4 + 2 * max_tokens * 4 : 0;
+  L.smem = L.off_seg + max_tokens * 16 + F8_EPI_GROUPS * 4 * 64 * 4 + 2 * max_tokens * 4 + hist_bytes + 1024;
   L.acc_cols = 32;
   while (L.acc_cols < n_max_rows) L.acc_cols <<= 1;
   L.n_acc = F8_TMEM_COLS / L.acc_cols < F8_MAX_ACC ? F8_TMEM_COLS / L.acc_cols : F8_MAX_ACC;
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
 indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int n_tok,
                    const int32_t* __restrict__ req_of, const int32_t* __restrict__ limit_of,
                    const uint8_t* __restrict__ qg, const float* __restrict__ wg, long long* __restrict__ keys_out,
-                   float* __restrict__ scores_out, int ld, F8Layout L) {
+                   float* __restrict__ scores_out, int ld, F8Layout L, uint32_t* __restrict__ hist0) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NS = L.stages;
@@ -118,6 +121,9 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
   float* s_w = reinterpret_cast<float*>(segs + D.max_tokens);     // [F8_EPI_GROUPS][4][64]
   int32_t* s_req = reinterpret_cast<int32_t*>(s_w + F8_EPI_GROUPS * 4 * 64);   // [n_tok]
   int32_t* s_lim = s_req + D.max_tokens;                          // [n_tok]
+  // hist0 (one query token, wide selection): the selection's level-0 histogram of
+  // this CTA's keys, added to the selection's global sums at the end
+  uint32_t* s_hist = hist0 ? reinterpret_cast<uint32_t*>(smem + L.off_hist) : nullptr;   // [SEL_BINS]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hi = D.n_idx_heads;
@@ -128,6 +134,8 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     for (int b = 0; b < F8_N_BARS; ++b) mbar_init(smem_u32(&bars[b]), 1);
     fence_mbar_init();
   }
+  if (s_hist)
+    for (int b = tid; b < SEL_BINS; b += F8_THREADS) s_hist[b] = 0;
   griddep_wait();
   griddep_launch();
   // ---- request segments of the batch (tokens of one request are contiguous) ----
@@ -351,8 +359,10 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
           }
         const float s = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * scale + 0.f;   // + 0: a zero score is +0
         if (ok && key < lim) {
-          keys_out[(size_t)(S.first + j) * ld + key] = f32_order_key(s);
+          const long long ok32 = f32_order_key(s);
+          keys_out[(size_t)(S.first + j) * ld + key] = ok32;
           if (scores_out) scores_out[(size_t)(S.first + j) * ld + key] = s;
+          if (s_hist) atomicAdd(&s_hist[bucket_of(sel_key(ok32, key), true)], 1u);
         }
       }
       tc_fence_before();
@@ -362,6 +372,11 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
         f8_arrive(smem_u32(&t_empty[tb]));
         f8_arrive(smem_u32(&c_empty[cs]));
       }
+    }
+    if (s_hist) {   // both warpgroups are done: this CTA's histogram to the global sums
+      f8_named_sync(4, F8_EPI_GROUPS * 128);
+      for (int b = tid; b < SEL_BINS; b += F8_EPI_GROUPS * 128)
+        if (s_hist[b]) atomicAdd(&hist0[b], s_hist[b]);
     }
   }
   __syncthreads();
@@ -380,9 +395,9 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
 
 hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
                              const uint8_t* d_q, const float* d_w, int64_t* d_keys, float* d_scores,
-                             cudaStream_t st) {
+                             uint32_t* d_hist0, cudaStream_t st) {
   const int n_max = ((p->cfg.max_q_per_req * p->cfg.n_idx_heads) + 15) & ~15;
-  const F8Layout L = f8_layout(n_max, p->cfg.max_tokens);
+  const F8Layout L = f8_layout(n_max, p->cfg.max_tokens, d_hist0 != nullptr);
   // alternate tiles go to alternate epilogue warpgroups: an even accumulator count
   // keeps every accumulator with one warpgroup, so its phase waits never alias
   if (L.stages < 2 || L.n_acc % F8_EPI_GROUPS || il < 0 || il >= (int)p->idx_tmaps.size()) return HS_ERR_INVALID;
@@ -394,7 +409,7 @@ hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, co
   }
   return launch_pdl(indexer_fp8_kernel, dim3(num_sms()), dim3(F8_THREADS), L.smem, st, 0, p->d, p->idx_tmaps[il],
                     il, n, d_req, d_limit, d_q, d_w, reinterpret_cast<long long*>(d_keys), d_scores,
-                    p->cfg.max_ctx, L);
+                    p->cfg.max_ctx, L, d_hist0);
 }
 
 }  // namespace hs

@@ -415,17 +415,27 @@ inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 // ---- host-side launch helpers (defined in hs_pool.cu) ----------------------------
+// d_hist0: nullable; the selection's level-0 histogram sums, which the scoring
+// kernel fills when the selection runs wide for one query token (select_hist0)
 hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
-                         const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, cudaStream_t st);
+                         const int8_t* d_q, const int8_t* d_w, int64_t* d_scores, uint32_t* d_hist0,
+                         cudaStream_t st);
+// CTAs per query token of the wide selection of n tokens (0: the cluster selection)
+int select_wide_groups(hs_pool* p, int n, bool wide_ok);
+// The level-0 histogram sums the scoring kernel fills for a wide one-token selection, else null.
+uint32_t* select_hist0(hs_pool* p, int n, bool wide_ok);
 // fp_keys: the scores are order-preserving keys of fp32 scores (FP8 indexer);
-// wide_ok: the pool's selection scratch may be used (few tokens: the wide kernel)
+// wide_ok: the pool's selection scratch may be used (few tokens: the wide kernel);
+// hist0_done: the scoring kernel filled select_hist0()
 hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                        int32_t* d_topk, cudaStream_t st, bool fp_keys = false, bool wide_ok = true);
+                        int32_t* d_topk, cudaStream_t st, bool fp_keys = false, bool wide_ok = true,
+                        bool hist0_done = false);
 hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* d_req,
                          const int32_t* d_topk, int32_t* d_row_ids, hs_plan_entry* d_plan,
                          cudaStream_t st);
 hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
-                             const uint8_t* d_q, const float* d_w, int64_t* d_keys, float* d_scores, cudaStream_t st);
+                             const uint8_t* d_q, const float* d_w, int64_t* d_keys, float* d_scores,
+                             uint32_t* d_hist0, cudaStream_t st);
 hs_status launch_replay(hs_pool* p, int group, int n, const int32_t* d_req, const int32_t* d_topk,
                         int32_t* d_row_ids, cudaStream_t st);
 // settled: d_rows and the rows it names were written before the previous kernel of

@@ -64,7 +64,7 @@ extern "C" hs_status hs_indexer_topk_noalloc(hs_pool* p, int32_t index_layer, in
   if (s != HS_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int64_t* scores = static_cast<int64_t*>(scratch);
-  s = launch_indexer(p, index_layer, n, d_req, d_limit, d_q, d_w, scores, st);
+  s = launch_indexer(p, index_layer, n, d_req, d_limit, d_q, d_w, scores, nullptr, st);
   if (s != HS_OK) return s;
   // the cluster selection: it needs no pool-owned scratch
   return launch_select(p, n, scores, p->cfg.max_ctx, d_limit, d_topk, st, false, false);

@@ -368,9 +368,10 @@ hs_status hs_indexer_topk(hs_pool* p, int32_t index_layer, int32_t n, const int3
   if (p->d.idx_fmt != HS_IDX_INT8) return HS_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int64_t* scores = d_scores ? d_scores : p->d.scores;
-  hs_status s = launch_indexer(p, index_layer, n, d_req, d_limit, d_q, d_w, scores, st);
+  uint32_t* hist0 = select_hist0(p, n, true);
+  hs_status s = launch_indexer(p, index_layer, n, d_req, d_limit, d_q, d_w, scores, hist0, st);
   if (s != HS_OK) return s;
-  return launch_select(p, n, scores, p->cfg.max_ctx, d_limit, d_topk, st);
+  return launch_select(p, n, scores, p->cfg.max_ctx, d_limit, d_topk, st, false, true, hist0 != nullptr);
 }
 
 hs_status hs_indexer_topk_fp8(hs_pool* p, int32_t index_layer, int32_t n, const int32_t* d_req,
@@ -384,9 +385,10 @@ hs_status hs_indexer_topk_fp8(hs_pool* p, int32_t index_layer, int32_t n, const 
     return HS_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the kernel writes each score as an order-preserving integer for the selection
-  hs_status s = launch_indexer_fp8(p, index_layer, n, d_req, d_limit, d_q, d_w, p->d.scores, d_scores, st);
+  uint32_t* hist0 = select_hist0(p, n, true);
+  hs_status s = launch_indexer_fp8(p, index_layer, n, d_req, d_limit, d_q, d_w, p->d.scores, d_scores, hist0, st);
   if (s != HS_OK) return s;
-  return launch_select(p, n, p->d.scores, p->cfg.max_ctx, d_limit, d_topk, st, true);
+  return launch_select(p, n, p->d.scores, p->cfg.max_ctx, d_limit, d_topk, st, true, true, hist0 != nullptr);
 }
 
 hs_status hs_resolve_topk(hs_pool* p, int32_t group, int32_t step, int32_t n, const int32_t* d_req,

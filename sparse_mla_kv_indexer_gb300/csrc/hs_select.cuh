@@ -113,7 +113,8 @@ inline int sel_wide_min_g(int max_ctx) {
   return g > SW_MIN_G ? g : SW_MIN_G;
 }
 
+// hist0_done: the level-0 histogram sums of the (single) token are already complete
 hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                             int32_t* d_topk, bool fp_keys, int G, cudaStream_t st);
+                             int32_t* d_topk, bool fp_keys, int G, bool hist0_done, cudaStream_t st);
 
 }  // namespace hs

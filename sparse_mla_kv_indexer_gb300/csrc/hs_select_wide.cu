@@ -19,6 +19,9 @@
 //    (the K-th largest key) in the list by itself, adds the counts of the CTAs
 //    before it to get its output offset, and writes its selected tokens in order.
 //  * After the last barrier each CTA clears a share of the sums for the next launch.
+//  * With a single query token the scoring kernel adds its CTAs' level-0 histograms
+//    to the sums as it writes the scores (hist0_done), so the selection starts from
+//    complete sums: no histogram pass over its chunk and no first barrier.
 // Its successor may start launching only once every CTA is resident (after the
 // first barrier), so a dependent kernel cannot take the SM a CTA still waits for.
 #include "hs_select.cuh"
@@ -98,7 +101,7 @@ __device__ __forceinline__ bool in_range(unsigned long long k, unsigned long lon
 
 __global__ void __launch_bounds__(SW_THREADS, 1)
 select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of,
-                   int32_t* __restrict__ topk, int fp_keys, int G) {
+                   int32_t* __restrict__ topk, int fp_keys, int G, int hist0_done) {
   const int tok = blockIdx.x / G, g = blockIdx.x - tok * G;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int K = D.topk;
@@ -125,8 +128,15 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   int n = limit_of[tok];
   n = max(0, min(n, D.max_ctx));
   int32_t* out = topk + (size_t)tok * K;
+  // a launch that returns before the barriers clears the sums the scoring kernel filled
+  auto clear_hist0 = [&]() {
+    if (hist0_done)
+      for (int b = g * (SEL_BINS / G + 1) + tid; b < min(SEL_BINS, (g + 1) * (SEL_BINS / G + 1)); b += SW_THREADS)
+        W->hist[0][b] = 0;
+  };
   if (n <= K) {   // every earlier token is selected (the same for all CTAs of the token)
     griddep_launch();
+    clear_hist0();
     if (g == 0)
       for (int i = tid; i < K; i += SW_THREADS) out[i] = i < n ? i : -1;
     return;
@@ -134,6 +144,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   const int per = ((n + G - 1) / G + 1) & ~1;   // even: every chunk starts 16-byte aligned
   if (per > SW_CHUNK) {   // the launch sizes G so that this cannot happen; same for all CTAs of the token
     griddep_launch();
+    clear_hist0();
     if (g == 0 && tid == 0) set_status(D.status, HS_ERR_BAD_ID);
     return;
   }
@@ -161,14 +172,18 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     }
     const unsigned long long k = sel_key(v, lo + i);
     cache[i] = k;
-    atomicAdd(&hist[bucket_of(k, fp_keys)], 1u);
+    if (!hist0_done) atomicAdd(&hist[bucket_of(k, fp_keys)], 1u);
   }
-  __syncthreads();
-  for (int b = tid; b < SEL_BINS; b += SW_THREADS)
-    if (hist[b]) atomicAdd(&W->hist[0][b], hist[b]);
-  unsigned long long nbar = 1;
-  if (!sw_barrier(&W->bar, bar0 + nbar * G, D.status, &s_ok)) return;
-  griddep_launch();   // every CTA of the token is resident
+  unsigned long long nbar = 0;
+  bool resident = false;   // every CTA of the token has passed a barrier: all are resident
+  if (!hist0_done) {
+    __syncthreads();
+    for (int b = tid; b < SEL_BINS; b += SW_THREADS)
+      if (hist[b]) atomicAdd(&W->hist[0][b], hist[b]);
+    if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
+    griddep_launch();
+    resident = true;
+  }
 
   // ---- narrow the range holding the K-th largest key, level by level ----
   int need = K;
@@ -193,6 +208,10 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     for (int b = tid; b < SEL_BINS; b += SW_THREADS)
       if (hist[b]) atomicAdd(&W->hist[level][b], hist[b]);
     if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
+    if (!resident) {
+      griddep_launch();
+      resident = true;
+    }
     sw_find<true>(W->hist[level], need, warp_tot, &s_bin, &s_above);
     n_range = (int)__ldcg(&W->hist[level][s_bin]);
     base += (unsigned long long)s_bin << shift;
@@ -232,6 +251,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     }
   }
   if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
+  if (!resident) griddep_launch();
   // every CTA has read the sums and appended its keys: clear a share of what
   // this launch used, and record where the next launch's barriers start
   {
@@ -311,8 +331,9 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
 }  // namespace
 
 hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                             int32_t* d_topk, bool fp_keys, int G, cudaStream_t st) {
-  if (G < 1 || G > SW_MAX_G || n < 1 || n > p->d.sel_ws_tokens || n * G > num_sms()) return HS_ERR_INVALID;
+                             int32_t* d_topk, bool fp_keys, int G, bool hist0_done, cudaStream_t st) {
+  if (G < 1 || G > SW_MAX_G || n < 1 || n > p->d.sel_ws_tokens || n * G > num_sms() || (hist0_done && n != 1))
+    return HS_ERR_INVALID;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(select_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SW_SMEM) !=
@@ -321,7 +342,7 @@ hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, c
     attr = true;
   }
   return launch_pdl(select_wide_kernel, dim3(n * G), dim3(SW_THREADS), SW_SMEM, st, 0, p->d, scores, ld, d_limit,
-                    d_topk, fp_keys ? 1 : 0, G);
+                    d_topk, fp_keys ? 1 : 0, G, hist0_done ? 1 : 0);
 }
 
 }  // namespace hs

@@ -3,9 +3,11 @@
 Key caches are built so that the scores are crowded: every key equal (all scores
 tie, the K lowest token ids win), all scores zero, three distinct scores over
 262,144 tokens, and plain random keys. Each runs with 1 and 2 query tokens (the
-wide selection, one group of CTAs per token over the whole GPU), with 8 query
-tokens (the cluster selection) and through hs_indexer_topk_noalloc (the cluster
-selection, no pool scratch); ragged limits and a limit below K are included.
+wide selection, one group of CTAs per token over the whole GPU; with one token the
+scoring kernel fills the selection's first histogram), with 8 query tokens (the
+cluster selection) and through hs_indexer_topk_noalloc (the cluster selection, no
+pool scratch); ragged limits and limits below K are included, and a one-token call
+with every token selected is followed by a full one (its sums must have been cleared).
 The oracle's top-K (vLLM blog Part 1, "Sparsity when you need it"; ties to the
 lower token index) is a full sort of the exact int64 scores.
 """
@@ -49,12 +51,14 @@ def _queries(kind, n_tok, rng):
     return q, w
 
 
-# (request of each token, limit of each token)
-BATCHES = {
-    1: ([0], [CTX]),
-    2: ([0, 1], [CTX - 1000, 131073]),
-    8: ([0, 0, 0, 0, 1, 1, 1, 1], [200001, 200002, 200003, 200004, 1000, 1001, K + 1, CTX]),
-}
+# (request of each token, limit of each token), run in this order
+BATCHES = [
+    ([0], [CTX]),
+    ([0], [1500]),
+    ([0], [CTX - 77]),
+    ([0, 1], [CTX - 1000, 131073]),
+    ([0, 0, 0, 0, 1, 1, 1, 1], [200001, 200002, 200003, 200004, 1000, 1001, K + 1, CTX]),
+]
 
 
 @pytest.mark.parametrize("kind", ["equal", "zero", "three", "random"])
@@ -75,7 +79,8 @@ def test_selection_matches_full_sort(kind):
     try:
         for r in range(2):
             pool.set_pages(r, 0, idx_pages=list(range(pages)))
-        for n_tok, (reqs, limits) in BATCHES.items():
+        for reqs, limits in BATCHES:
+            n_tok = len(reqs)
             q, w = _queries(kind, n_tok, rng)
             want = np.stack([OI.topk(OI.scores(q[i], w[i], keys[:limits[i]]), K) for i in range(n_tok)])
             d_req = torch.tensor(reqs, dtype=torch.int32, device="cuda")
