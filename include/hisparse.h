@@ -29,6 +29,14 @@
  *   timed-out wait) are recorded in a device status word and reported by
  *   hs_get_error, which synchronises the stream. A call that finds a bad
  *   argument on the host returns HS_ERR_INVALID and launches nothing.
+ * - Programmatic dependent launch: a hot-path kernel may start while the previous
+ *   kernel of the stream finishes, and waits for it before it reads that kernel's
+ *   output. Request ids (d_req), causal limits (d_limit), the block tables and the
+ *   hot-buffer state are read before that wait, so they must be final before the
+ *   previous kernel started. That holds for values written by the host (copies are
+ *   stream-ordered), by this library's own calls (none writes them in a kernel) and
+ *   by any ordinary kernel launch; it does not hold for a kernel that itself lets
+ *   its dependents start early (griddepcontrol.launch_dependents) and writes them.
  * - A query-token batch is described by per-token device arrays: d_req (the
  *   request slot of each token) and d_limit (causal limit: the token sees
  *   positions [0, limit)). The tokens of one request are contiguous in the

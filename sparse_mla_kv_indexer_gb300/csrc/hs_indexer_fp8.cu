@@ -136,8 +136,10 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
   }
   if (s_hist)
     for (int b = tid; b < SEL_BINS; b += F8_THREADS) s_hist[b] = 0;
-  griddep_wait();
-  griddep_launch();
+  // Request ids, limits and the index block table are final before the preceding
+  // kernel started: the segments and page ids are set up while it finishes. Each role
+  // waits for that kernel before it reads data it may have produced (keys, queries,
+  // weights); the score and histogram writes follow the key copies.
   // ---- request segments of the batch (tokens of one request are contiguous) ----
   for (int t = tid; t < n_tok; t += F8_THREADS) {
     int r = req_of[t], lim = limit_of[t];
@@ -205,6 +207,8 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     int c0, c1, n0, n1;
     fetch(lane, c0, c1);
     fetch(32 + lane, n0, n1);
+    griddep_wait();
+    griddep_launch();
     for (int i = 0; i < n_local; ++i) {
       if (i > 0 && (i & 31) == 0) {
         c0 = n0;
@@ -246,6 +250,7 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     }
   } else if (warp == F8_MMA_WARP) {
     // ------------------------------ MMA issuer ------------------------------
+    griddep_wait();   // the queries may come from the preceding kernel
     // lane 0 waits and issues; the warp's 32 lanes load each segment's queries
     int cur_seg = -1, nb = 0, any = 0;
     for (int i = 0; i < n_local; ++i) {
@@ -308,6 +313,7 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     }
   } else {
     // ------------------------------ epilogue ------------------------------
+    griddep_wait();   // the head weights may come from the preceding kernel
     const int grp = warp >> 2, et = tid & 127;          // warpgroup, thread within it
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     float* sw = s_w + grp * 4 * 64;
