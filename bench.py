@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "HiSparse decode tokens/s (1 GB300) + achieved HBM/host-link GB/s vs roofline"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -268,6 +269,51 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 tensor peak: the measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def host_link_probe(torch, H, reps=10):
+    """Host-link rates on this machine: single 656-byte rows read from pinned, mapped host
+    memory by hs_link_probe (the miss-copy pattern, 16,384 random rows of a 256 MB
+    host buffer), and bulk pinned copies H2D / D2H of 64 MB (cudaMemcpyAsync through
+    torch). Each the best of `reps` timed repetitions with CUDA events."""
+    rows_total = (256 << 20) // 656
+    host = torch.empty(rows_total * 656, dtype=torch.uint8, pin_memory=True)
+    host.fill_(1)
+    n = 16384
+    g = torch.Generator().manual_seed(0)
+    src = torch.randint(0, rows_total, (n,), generator=g, dtype=torch.int64).cuda()
+    dst = torch.empty(n * 656, dtype=torch.uint8, device="cuda")
+    bulk_h = torch.empty(64 << 20, dtype=torch.uint8, pin_memory=True)
+    bulk_d = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+
+    def best(fn, nbytes):
+        fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b) / 1000.0)
+        return nbytes / min(t) / 1e9
+
+    single = best(lambda: H.link_probe(host, 656, src, dst), n * 656)
+    h2d = best(lambda: bulk_d.copy_(bulk_h, non_blocking=True), bulk_h.numel())
+    d2h = best(lambda: bulk_h.copy_(bulk_d, non_blocking=True), bulk_h.numel())
+    return {"single_row_gbs": single, "h2d_gbs": h2d, "d2h_gbs": d2h,
+            "how": "hs_link_probe: 16,384 random 656-byte rows from a 256 MB pinned mapped buffer; "
+                   "bulk: 64 MB pinned copies; best of 10, CUDA events"}
 
 
 def sources_sha256(files):
@@ -523,7 +569,21 @@ def main():
     achieved = dom_bytes / (avg_ms / 1000.0) / 1e9 if avg_ms > 0 else 0.0
     tkey = dom + "_fp8" if dom == "indexer_topk" and cfg.idx_fp8 else dom   # key of the committed traffic
     step_bytes = alg["indexer_topk"] * cfg.n_groups + alg["sparse_mla_decode"] * cfg.n_layers
-    roof_step_s = step_bytes / (peak * 1e9)
+    # step roofline: HBM bytes at the measured copy rate plus miss bytes at the measured
+    # single-row host-link rate, or the tensor term (attention 2,176 FLOP per row per head,
+    # vLLM blog Part 2 footnote 1; indexer 2 x 128 x H_i per key per query token, run as
+    # fp16/fp8 MMAs) when larger
+    from sparse_mla_kv_indexer_gb300 import hisparse as HS
+    link = host_link_probe(torch, HS)
+    miss_bytes = counters.h2d_bytes / K
+    n_tok = len(plans[Wm].tokens)
+    keys_scored = alg["indexer_topk"] / (132 if cfg.idx_fp8 else 128)
+    flops = (n_tok * cfg.n_layers * cfg.topk * cfg.n_heads * 2176.0 +
+             keys_scored * cfg.n_groups * cfg.t_q * 2.0 * 128 * cfg.n_idx_heads)
+    tflops, tflops_kind = measured_bf16_tflops()
+    t_mem = step_bytes / (peak * 1e9) + miss_bytes / (link["single_row_gbs"] * 1e9)
+    t_tensor = flops / (tflops * 1e12)
+    roof_step_s = max(t_mem, t_tensor)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -543,13 +603,22 @@ def main():
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "traffic": ncu_traffic(KERNEL_FILES.get(tkey, []), tkey, args.workload)},
-        "step_roofline": {"algorithmic_hbm_bytes": step_bytes, "roofline_ms": roof_step_s * 1e3,
-                          "frac": roof_step_s / (t_max / K)},
+        "step_roofline": {"algorithmic_hbm_bytes": step_bytes, "miss_bytes": miss_bytes,
+                          "host_link_gbs": link["single_row_gbs"], "tensor_flops": flops,
+                          "tensor_peak_tflops": tflops, "tensor_peak_source": tflops_kind,
+                          "bound": "hbm+link" if t_mem >= t_tensor else "tensor",
+                          "roofline_ms": roof_step_s * 1e3, "frac": roof_step_s / (t_max / K)},
+        "host_link": link,
         "breakdown_ms_per_call": {k: v["ms"] for k, v in calls.items()},
         "calls_per_step": {k: v["per_step"] for k, v in calls.items()},
         "timing": "each timed step is one CUDA graph replay; per-call times from single-call graphs",
         "resolver": {"hits": counters.hits / K, "misses": counters.misses / K, "resident": counters.resident / K,
-                     "h2d_bytes_per_step": counters.h2d_bytes / K, "d2h_bytes_per_step": counters.d2h_bytes / K},
+                     "h2d_bytes_per_step": counters.h2d_bytes / K, "d2h_bytes_per_step": counters.d2h_bytes / K,
+                     # the miss bytes of a step at the probe's single-row rate, against the
+                     # resolver's whole call time (classification included)
+                     "miss_link_us_per_step": miss_bytes / (link["single_row_gbs"] * 1e9) * 1e6,
+                     "resolve_us_per_step": (calls["resolve_topk"]["ms"] * calls["resolve_topk"]["per_step"] * 1e3
+                                             if "resolve_topk" in calls else None)},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": statistics.mean(host_sess.h2d_bytes),
                 "d2h_bytes_per_step": host_sess.d2h_bytes},
         "gpu_launches": launches,

@@ -304,6 +304,22 @@ hs_status hs_get_counters(hs_pool* pool, hs_counters* out, int32_t reset, hs_str
 /* Static text for a status code. */
 const char* hs_status_string(hs_status s);
 
+/* Host-link probe (a measurement aid, not part of the decode step and needing no
+ * pool): copies n single rows of row_bytes from pinned, mapped host memory into
+ * d_dst, row i taken from host row d_src_rows[i], 16 bytes per thread with four
+ * loads in flight, the access pattern of the resolver's miss copies. Timing it
+ * gives the host-link rate for single-row reads that the step roofline charges
+ * miss bytes against ([P1] "How it works": a miss copies one row from pinned host
+ * memory).
+ *  h_mapped: pinned host memory allocated mapped (cudaHostAllocMapped, or a
+ *  PyTorch pinned tensor), n_host_rows rows of row_bytes, 16-byte aligned;
+ *  row_bytes a positive multiple of 16; d_src_rows [n] int64, an index outside
+ *  [0, n_host_rows) leaves its destination row unchanged; d_dst
+ *  [n * row_bytes], 16-byte aligned. HS_ERR_INVALID for a null or misaligned
+ *  pointer, a bad size, or host memory that is not mapped. Asynchronous. */
+hs_status hs_link_probe(const void* h_mapped, int64_t n_host_rows, int32_t row_bytes, const int64_t* d_src_rows,
+                        int64_t n, void* d_dst, hs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -128,6 +128,35 @@ __global__ void clear_hot_kernel(Dev D, int r) {
   }
 }
 
+// Host-link probe: n single rows from mapped host memory, 16 B per thread, four
+// loads in flight per thread (the resolver's miss-copy pattern).
+__global__ void __launch_bounds__(256) link_probe_kernel(const uint8_t* __restrict__ src, long long n_src_rows,
+                                                         int row_bytes, const int64_t* __restrict__ rows,
+                                                         long long n, uint8_t* __restrict__ dst) {
+  const int chunks = row_bytes / 16;
+  const long long total = n * chunks;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long c0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; c0 < total; c0 += 4 * stride) {
+    uint4 v[4];
+    long long at[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long c = c0 + u * stride;
+      at[u] = -1;
+      if (c >= total) continue;
+      const long long i = c / chunks;
+      const int part = (int)(c - i * chunks);
+      const long long r = rows[i];
+      if (r < 0 || r >= n_src_rows) continue;
+      v[u] = *reinterpret_cast<const uint4*>(src + (size_t)r * row_bytes + part * 16);
+      at[u] = (long long)i * row_bytes + part * 16;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (at[u] >= 0) *reinterpret_cast<uint4*>(dst + at[u]) = v[u];
+  }
+}
+
 int launch_blocks(long long work, int threads) {
   long long b = (work + threads - 1) / threads;
   long long cap = 4ll * num_sms();
@@ -433,6 +462,23 @@ hs_status hs_offload_pages(hs_pool* p, int32_t n, const int32_t* d_pool_pages, c
   const long long work = (long long)n * p->d.n_layers * (PAGE * ROW / 16);
   return launch_pdl(offload_kernel, dim3(launch_blocks(work, 256)), dim3(256), 0,
                     reinterpret_cast<cudaStream_t>(stream), 0, p->d, n, d_pool_pages, d_host_pages);
+}
+
+hs_status hs_link_probe(const void* h_mapped, int64_t n_host_rows, int32_t row_bytes, const int64_t* d_src_rows,
+                        int64_t n, void* d_dst, hs_stream_t stream) {
+  if (!h_mapped || !d_src_rows || !d_dst || n < 0 || n_host_rows < 1 || row_bytes < 16 || row_bytes % 16 ||
+      !aligned16(d_dst) || !aligned16(h_mapped))
+    return HS_ERR_INVALID;
+  if (n == 0) return HS_OK;
+  void* src = nullptr;
+  if (cudaHostGetDevicePointer(&src, const_cast<void*>(h_mapped), 0) != cudaSuccess || !aligned16(src)) {
+    cudaGetLastError();
+    return HS_ERR_INVALID;
+  }
+  const long long work = n * (row_bytes / 16);
+  link_probe_kernel<<<launch_blocks((work + 3) / 4, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(src), n_host_rows, row_bytes, d_src_rows, n, static_cast<uint8_t*>(d_dst));
+  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
 hs_status hs_get_error(hs_pool* p, hs_status* device_status, hs_stream_t stream) {

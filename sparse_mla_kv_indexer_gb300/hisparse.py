@@ -65,6 +65,7 @@ _SIGS = {
     "hs_offload_pages": [_P, _I, _P, _P, _P],
     "hs_get_error": [_P, ctypes.POINTER(ctypes.c_int), _P],
     "hs_get_counters": [_P, ctypes.POINTER(Counters), _I, _P],
+    "hs_link_probe": [_P, ctypes.c_int64, _I, _P, ctypes.c_int64, _P, _P],
 }
 
 
@@ -111,6 +112,13 @@ def _host_array(values, ctype):
         return None
     arr = (ctype * len(values))(*[int(v) for v in values])
     return ctypes.cast(arr, _P), arr
+
+
+def link_probe(host_rows, row_bytes: int, src_rows, dst, stream=None) -> None:
+    """hs_link_probe: copy dst[i] = host row src_rows[i] (single-row reads from a
+    pinned, mapped host tensor), the access pattern of the resolver's miss copies."""
+    _check("hs_link_probe", lib.hs_link_probe(_ptr(host_rows), host_rows.numel() * host_rows.element_size() // row_bytes,
+                                              row_bytes, _ptr(src_rows), src_rows.numel(), _ptr(dst), _stream(stream)))
 
 
 class Pool:
