@@ -30,13 +30,16 @@
  *   hs_get_error, which synchronises the stream. A call that finds a bad
  *   argument on the host returns HS_ERR_INVALID and launches nothing.
  * - Programmatic dependent launch: a hot-path kernel may start while the previous
- *   kernel of the stream finishes, and waits for it before it reads that kernel's
- *   output. Request ids (d_req), causal limits (d_limit), the block tables and the
+ *   kernel of the stream finishes, and waits for it before it reads the outputs of
+ *   earlier calls of this library (scores, top-K, row ids, KV rows and index keys).
+ *   A call's own input arrays (d_req, d_limit, d_pos, the rows and keys to append,
+ *   the indexer's d_q and d_w, the attention's d_q), the block tables and the
  *   hot-buffer state are read before that wait, so they must be final before the
  *   previous kernel started. That holds for values written by the host (copies are
  *   stream-ordered), by this library's own calls (none writes them in a kernel) and
- *   by any ordinary kernel launch; it does not hold for a kernel that itself lets
- *   its dependents start early (griddepcontrol.launch_dependents) and writes them.
+ *   by any ordinary kernel launch, which lets no dependent start before it ends; it
+ *   does not hold for a kernel that itself lets its dependents start early
+ *   (griddepcontrol.launch_dependents) and writes them afterwards.
  * - A query-token batch is described by per-token device arrays: d_req (the
  *   request slot of each token) and d_limit (causal limit: the token sees
  *   positions [0, limit)). The tokens of one request are contiguous in the
@@ -251,8 +254,8 @@ hs_status hs_replay_topk(hs_pool* pool, int32_t group, int32_t n_tokens, const i
  *  pointers or out-of-range arguments).
  *  Layers of one selection: when the previous launch of this pool was
  *  hs_sparse_mla_decode with the same d_row_ids on the same stream, the kernel
- *  reads the row ids and gathers the rows while that kernel finishes
- *  (programmatic dependent launch) and reads d_q only after it completes.
+ *  also reads the row ids and gathers the rows while that kernel finishes
+ *  (programmatic dependent launch).
  *  Between two such calls, d_row_ids and the KV rows may change only through
  *  stream work that is not a programmatic-dependent kernel (an ordinary kernel
  *  launch, a copy or a memset). Any other call of this library on the pool ends

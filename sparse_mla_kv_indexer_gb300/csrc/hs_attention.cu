@@ -171,9 +171,18 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     fence_mbar_init();
   }
   if constexpr (PL::DSM) cluster_arrive_relaxed();   // this CTA has started; its barriers are initialised
-  // Settled: the row ids and the rows were written before the kernel this one
-  // follows (an earlier layer of the same selection), so they are read while that
-  // kernel finishes, through L2; q may come from that kernel and waits for it.
+  // q is an input of the call, final before the preceding kernel started: it is
+  // loaded while that kernel finishes. Settled: the row ids and the rows were
+  // written before it too (an earlier layer of the same selection), so they are
+  // gathered meanwhile as well, through L2.
+  const uint16_t* qt = q + ((size_t)tok * H + (size_t)hgrp * HPC) * QK;
+  constexpr int QPT = (HPC * 72 + AT_THREADS - 1) / AT_THREADS;
+  uint4 qv[QPT];
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int c = tid + k * AT_THREADS;
+    qv[k] = c < HPC * 72 ? __ldg(reinterpret_cast<const uint4*>(qt) + c) : make_uint4(0, 0, 0, 0);
+  }
   if (!settled) {
     griddep_wait();
     griddep_launch();
@@ -185,28 +194,7 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     if (id >= max_row) { set_status(D.status, HS_ERR_BAD_ID); id = -1; }
     ids[tid] = id;
   }
-  // ---- Q: this head group's [HPC, 576] bf16, 72 chunks of 8 per head, loads in flight ----
-  const uint16_t* qt = q + ((size_t)tok * H + (size_t)hgrp * HPC) * QK;
-  constexpr int QPT = (HPC * 72 + AT_THREADS - 1) / AT_THREADS;
-  uint4 qv[QPT];
-  auto load_q = [&]() {
-#pragma unroll
-    for (int k = 0; k < QPT; ++k) {
-      const int c = tid + k * AT_THREADS;
-      qv[k] = c < HPC * 72 ? __ldg(reinterpret_cast<const uint4*>(qt) + c) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  auto place_q = [&]() {
-#pragma unroll
-    for (int k = 0; k < QPT; ++k) {
-      const int c = tid + k * AT_THREADS;
-      if (c < HPC * 72) {
-        const int h = c / 72, ch = c - h * 72;
-        *reinterpret_cast<uint4*>(Qs + (ch >> 3) * PL::Q_COL + sw128_chunk(h, ch & 7)) = qv[k];
-      }
-    }
-  };
-  if (!settled) load_q();
+  // ---- Q: this head group's [HPC, 576] bf16, 72 chunks of 8 per head (loaded above) ----
   __syncthreads();   // ids ready
   // ---- all row chunks in flight at once: chunk c = row * 41 + part ----
   uint4 rc[AT_CPT];
@@ -223,7 +211,14 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
       }
     }
   }
-  if (!settled) place_q();
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int c = tid + k * AT_THREADS;
+    if (c < HPC * 72) {
+      const int h = c / 72, ch = c - h * 72;
+      *reinterpret_cast<uint4*>(Qs + (ch >> 3) * PL::Q_COL + sw128_chunk(h, ch & 7)) = qv[k];
+    }
+  }
 #pragma unroll
   for (int k = 0; k < AT_CPT; ++k) {
     const int c = tid + k * AT_THREADS;
@@ -247,8 +242,6 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   if (settled) {
     griddep_wait();
     griddep_launch();
-    load_q();
-    place_q();
   }
   fence_proxy_async();
   tc_fence_before();

@@ -170,10 +170,11 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   }
   if (s_hist)
     for (int b = tid; b < SEL_BINS; b += IX_THREADS) s_hist[b] = 0;
-  // Request ids, limits and the index block table are final before the preceding
-  // kernel started: the segments and page ids are set up while it finishes. Each role
-  // waits for that kernel before it reads data it may have produced (keys, queries,
-  // weights); the score and histogram writes follow the key copies.
+  // Request ids, limits, queries, weights and the index block table are inputs,
+  // final before the preceding kernel started: the segments, page ids, query operand
+  // and weights are set up while it finishes. The producer waits for that kernel
+  // before its first key copy (the keys may have been appended by it); the score and
+  // histogram writes follow the copies.
   // ---- request segments of the batch (tokens of one request are contiguous) ----
   for (int t = tid; t < n_tok; t += IX_THREADS) {
     int r = req_of[t], lim = limit_of[t];
@@ -306,7 +307,6 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
     }
   } else if (warp >= IX_CONV_WARP0) {
     // ------------------------------ converters ------------------------------
-    griddep_wait();   // the queries may come from the preceding kernel
     const int ct = tid - IX_CONV_WARP0 * 32;
     int cur_seg = -1;
     for (int i = 0; i < n_local; ++i) {
@@ -384,7 +384,6 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
     }
   } else {
     // ------------------------------ epilogue ------------------------------
-    griddep_wait();   // the head weights may come from the preceding kernel
     // warpgroup grp takes tiles i = grp, grp + 2, ...; the accumulator count is even,
     // so each accumulator stays with one warpgroup and its phase waits never alias
     const int grp = warp >> 2, et = tid & 127;

@@ -136,10 +136,11 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
   }
   if (s_hist)
     for (int b = tid; b < SEL_BINS; b += F8_THREADS) s_hist[b] = 0;
-  // Request ids, limits and the index block table are final before the preceding
-  // kernel started: the segments and page ids are set up while it finishes. Each role
-  // waits for that kernel before it reads data it may have produced (keys, queries,
-  // weights); the score and histogram writes follow the key copies.
+  // Request ids, limits, queries, weights and the index block table are inputs,
+  // final before the preceding kernel started: the segments, page ids, query operand
+  // and weights are set up while it finishes. The producer waits for that kernel
+  // before its first key copy (the keys may have been appended by it); the score and
+  // histogram writes follow the copies.
   // ---- request segments of the batch (tokens of one request are contiguous) ----
   for (int t = tid; t < n_tok; t += F8_THREADS) {
     int r = req_of[t], lim = limit_of[t];
@@ -250,7 +251,6 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     }
   } else if (warp == F8_MMA_WARP) {
     // ------------------------------ MMA issuer ------------------------------
-    griddep_wait();   // the queries may come from the preceding kernel
     // lane 0 waits and issues; the warp's 32 lanes load each segment's queries
     int cur_seg = -1, nb = 0, any = 0;
     for (int i = 0; i < n_local; ++i) {
@@ -313,7 +313,6 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     }
   } else {
     // ------------------------------ epilogue ------------------------------
-    griddep_wait();   // the head weights may come from the preceding kernel
     const int grp = warp >> 2, et = tid & 127;          // warpgroup, thread within it
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     float* sw = s_w + grp * 4 * 64;
