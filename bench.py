@@ -438,6 +438,13 @@ def oracle_sample(name, seconds, rank=0):
     return toks / dt, f"{arm.next} consecutive decode steps of {name} ({toks} query tokens, {dt:.1f} s)", arm.cores
 
 
+def config_line(workload, cfg):
+    """The `config` object of a bench line (the same for both arms)."""
+    return {"workload": workload, "requests_per_gpu": cfg.n_requests, "context": list(cfg.ctx_len)[:4],
+            "heads": cfg.n_heads, "topk": cfg.topk, "sparse_layers": cfg.n_layers, "indexer_layers": cfg.n_groups,
+            "query_tokens_per_request": cfg.t_q, "l2": "flushed between timed steps (256 MB write)"}
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return 0
@@ -454,7 +461,7 @@ def reference_arm(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * sum(times) / max(1, len(times)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload},
+        "data": "synthetic", "config": config_line(args.workload, arm.cfg),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": arm.cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -595,10 +602,7 @@ def main():
         "ms_per_step": 1000.0 * t_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8->int64 (indexer, exact), fp8-e4m3/bf16->fp32 (attention)",
         "data": "synthetic",
-        "config": {"workload": args.workload, "requests_per_gpu": cfg.n_requests,
-                   "context": list(cfg.ctx_len)[:4], "heads": cfg.n_heads, "topk": cfg.topk,
-                   "sparse_layers": cfg.n_layers, "indexer_layers": cfg.n_groups,
-                   "query_tokens_per_request": cfg.t_q, "l2": "flushed between timed steps (256 MB write)"},
+        "config": config_line(args.workload, cfg),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes,
