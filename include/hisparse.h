@@ -16,6 +16,8 @@
  *
  * Conventions
  * - Every call returns an hs_status. No C++ exception crosses the ABI.
+ * - Every call opens an NVTX range named after it (inert unless a profiler is
+ *   attached), so a timeline shows the decode step call by call.
  * - "d_" pointers are device memory, "h_" pointers are host memory. The big
  *   buffers (KV pool tensors, index-key caches, pinned host pool) are owned by
  *   the caller and must outlive the pool. The library owns only the opaque
@@ -296,6 +298,12 @@ hs_status hs_offload_pages(hs_pool* pool, int32_t n, const int32_t* d_pool_pages
 hs_status hs_indexer_topk_noalloc(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
                                   const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
                                   const int8_t* d_w, int32_t* d_topk, hs_stream_t stream);
+
+/* Self-test of the failure path (not part of the decode step): one kernel waits,
+ * with the bounded wait every hot-path kernel uses, for an mbarrier arrival that
+ * never comes; after about one second it records HS_ERR_TIMEOUT in the device
+ * status word and returns, leaving the context usable. Asynchronous. */
+hs_status hs_wait_selftest(hs_pool* pool, hs_stream_t stream);
 
 /* Synchronise stream, return the first device-detected error since the last
  * call in *device_status and clear it. */

@@ -110,16 +110,6 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[HW]) {
   return v[0];
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
 
 template <int HPC>
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -144,8 +134,10 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   __half* recv = reinterpret_cast<__half*>(smem + PL::OFF_RECV);
   float* rstats = reinterpret_cast<float*>(smem + PL::OFF_STATS);
 
-  const uint32_t split = cluster_rank();
-  const uint32_t n_splits = cluster_size();
+  // the row splits of a (token, head group) are the x extent of the grid, one cluster
+  // when there are several; a single split (top-K <= 128) is launched without a cluster
+  const uint32_t split = blockIdx.x;
+  const uint32_t n_splits = gridDim.x;
   const int H = D.n_heads, K = D.topk;
   const int n_hgrp = H / HPC;
   const int tok = blockIdx.y / n_hgrp, hgrp = blockIdx.y - tok * n_hgrp;
@@ -170,7 +162,7 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     }
     fence_mbar_init();
   }
-  if constexpr (PL::DSM) cluster_arrive_relaxed();   // this CTA has started; its barriers are initialised
+  if (PL::DSM && n_splits > 1) cluster_arrive_relaxed();   // this CTA has started; its barriers are initialised
   // q is an input of the call, final before the preceding kernel started: it is
   // loaded while that kernel finishes. Settled: the row ids and the rows were
   // written before it too (an earlier layer of the same selection), so they are
@@ -371,7 +363,36 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     }
     umma_commit(smem_u32(bar + 1));
   }
-  if constexpr (PL::DSM) {
+  if (n_splits == 1) {
+    // ---- one split holds every selected row: its output, normalised by its own sum,
+    //      is final; no merge and no cluster instruction (the launch has no cluster) ----
+    if (tid < HPC) {
+      const float l = red[tid] + red[HPC + tid] + red[2 * HPC + tid] + red[3 * HPC + tid];
+      lfin[tid] = l;
+      gstat[tid] = l > 0.f ? (mfin[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+    ok &= mbar_wait(smem_u32(bar + 1), 0, D.status);
+    tc_fence_after();
+    __syncthreads();   // lfin
+    {
+      const int g = sub;
+      const int dim = g * 128 + quad * 32 + lane;   // warp (row quadrant, group g): one dim per lane
+      constexpr int CW = HPC < 32 ? HPC : 32;       // columns per TMEM read
+      uint16_t* o = out + ((size_t)tok * H + (size_t)hgrp * HPC) * 512 + dim;
+#pragma unroll
+      for (int h0 = 0; h0 < HPC; h0 += CW) {
+        uint32_t r[CW];
+        tmem_ld_cols<CW>(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 64 + h0), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          const float l = lfin[h0 + j];
+          o[(size_t)(h0 + j) * 512] = __bfloat16_as_ushort(__float2bfloat16_rn(l > 0.f ? __uint_as_float(r[j]) / l : 0.f));
+        }
+      }
+    }
+    if (lse_out && tid < HPC) lse_out[(size_t)tok * H + (size_t)hgrp * HPC + tid] = gstat[tid];
+  } else if constexpr (PL::DSM) {
     // while PV runs: this split's per-head (max, sum) into every CTA of the cluster
     cluster_wait_acquire();   // every CTA has started and initialised its barriers
     if (tid >= 128 && tid < 128 + HPC) {

@@ -15,6 +15,8 @@
 // made with that device current, and passed to the kernels.
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "hs_internal.cuh"
 
 using namespace hs;
@@ -50,6 +52,10 @@ hs_status scratch_address(int dev, void** out) {
 extern "C" hs_status hs_indexer_topk_noalloc(hs_pool* p, int32_t index_layer, int32_t n, const int32_t* d_req,
                                              const int32_t* d_limit, const int8_t* d_q, const int8_t* d_w,
                                              int32_t* d_topk, hs_stream_t stream) {
+  nvtxRangePushA("hs_indexer_topk_noalloc");
+  struct Pop {
+    ~Pop() { nvtxRangePop(); }
+  } pop;
   if (!p || index_layer < 0 || index_layer >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   if (n == 0) return HS_OK;
   if (!d_req || !d_limit || !d_q || !d_w || !d_topk || (reinterpret_cast<uintptr_t>(d_q) & 15)) return HS_ERR_INVALID;

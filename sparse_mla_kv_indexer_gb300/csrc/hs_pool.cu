@@ -12,6 +12,8 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "hs_select.cuh"
 
 using namespace hs;
@@ -157,6 +159,24 @@ __global__ void __launch_bounds__(256) link_probe_kernel(const uint8_t* __restri
   }
 }
 
+// One NVTX range per ABI call (host side; inert unless a profiler is attached).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+};
+
+// Self-test of the bounded device wait: an mbarrier expecting two arrivals gets one,
+// so the wait the hot-path kernels use runs out and records HS_ERR_TIMEOUT.
+__global__ void wait_selftest_kernel(Dev D) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 2);
+    fence_mbar_init();
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar)) : "memory");
+    mbar_wait(smem_u32(&bar), 0, D.status);   // the second arrival never comes
+  }
+}
+
 int launch_blocks(long long work, int threads) {
   long long b = (work + threads - 1) / threads;
   long long cap = 4ll * num_sms();
@@ -218,6 +238,7 @@ static hs_status make_key_tensor_maps(hs_pool* p, void* const* d_idx_layers) {
 
 hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void* const* d_idx_layers,
                        void* h_host_kv, hs_pool** out) {
+  CallRange nvtx_range("hs_pool_init");
   if (!cfg || !d_kv_layers || !d_idx_layers || !h_host_kv || !out) return HS_ERR_INVALID;
   *out = nullptr;
   const hs_pool_config& c = *cfg;
@@ -313,6 +334,7 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
 }
 
 hs_status hs_pool_destroy(hs_pool* pool) {
+  CallRange nvtx_range("hs_pool_destroy");
   if (!pool) return HS_ERR_INVALID;
   cudaDeviceSynchronize();
   for (void* a : pool->allocations) cudaFree(a);
@@ -322,6 +344,7 @@ hs_status hs_pool_destroy(hs_pool* pool) {
 
 hs_status hs_request_set_pages(hs_pool* p, int32_t req, int32_t first_page, int32_t n, const int32_t* h_block_table,
                                const int32_t* h_idx_pages, const int64_t* h_host_pages, hs_stream_t stream) {
+  CallRange nvtx_range("hs_request_set_pages");
   if (!p || req < 0 || req >= p->cfg.max_requests || first_page < 0 || n < 0 ||
       (long long)first_page + n > p->d.max_pages)
     return HS_ERR_INVALID;
@@ -345,6 +368,7 @@ hs_status hs_request_set_pages(hs_pool* p, int32_t req, int32_t first_page, int3
 
 hs_status hs_hot_lease(hs_pool* p, int32_t req, int32_t group, int32_t n, const int32_t* h_pool_pages,
                        hs_stream_t stream) {
+  CallRange nvtx_range("hs_hot_lease");
   if (!p || req < 0 || req >= p->cfg.max_requests || group < 0 || group >= p->d.n_groups || n < 0 ||
       (n > 0 && !h_pool_pages))
     return HS_ERR_INVALID;
@@ -365,6 +389,7 @@ hs_status hs_hot_lease(hs_pool* p, int32_t req, int32_t group, int32_t n, const 
 }
 
 hs_status hs_hot_release(hs_pool* p, int32_t req, hs_stream_t stream) {
+  CallRange nvtx_range("hs_hot_release");
   if (!p || req < 0 || req >= p->cfg.max_requests) return HS_ERR_INVALID;
   p->settled_rows = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -376,6 +401,7 @@ hs_status hs_hot_release(hs_pool* p, int32_t req, hs_stream_t stream) {
 
 hs_status hs_append_rows(hs_pool* p, int32_t n, const int32_t* d_req, const int32_t* d_pos, const uint8_t* d_kv_rows,
                          const int8_t* d_idx_keys, hs_stream_t stream) {
+  CallRange nvtx_range("hs_append_rows");
   if (!p || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
@@ -389,6 +415,7 @@ hs_status hs_append_rows(hs_pool* p, int32_t n, const int32_t* d_req, const int3
 hs_status hs_indexer_topk(hs_pool* p, int32_t index_layer, int32_t n, const int32_t* d_req, const int32_t* d_limit,
                           const int8_t* d_q, const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,
                           hs_stream_t stream) {
+  CallRange nvtx_range("hs_indexer_topk");
   if (!p || index_layer < 0 || index_layer >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
@@ -406,6 +433,7 @@ hs_status hs_indexer_topk(hs_pool* p, int32_t index_layer, int32_t n, const int3
 hs_status hs_indexer_topk_fp8(hs_pool* p, int32_t index_layer, int32_t n, const int32_t* d_req,
                               const int32_t* d_limit, const uint8_t* d_q, const float* d_w, int32_t* d_topk,
                               float* d_scores, hs_stream_t stream) {
+  CallRange nvtx_range("hs_indexer_topk_fp8");
   if (!p || index_layer < 0 || index_layer >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
@@ -422,6 +450,7 @@ hs_status hs_indexer_topk_fp8(hs_pool* p, int32_t index_layer, int32_t n, const 
 
 hs_status hs_resolve_topk(hs_pool* p, int32_t group, int32_t step, int32_t n, const int32_t* d_req,
                           const int32_t* d_topk, int32_t* d_row_ids, hs_plan_entry* d_plan, hs_stream_t stream) {
+  CallRange nvtx_range("hs_resolve_topk");
   if (!p || group < 0 || group >= p->d.n_groups || step < 0 || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
@@ -431,6 +460,7 @@ hs_status hs_resolve_topk(hs_pool* p, int32_t group, int32_t step, int32_t n, co
 
 hs_status hs_replay_topk(hs_pool* p, int32_t group, int32_t n, const int32_t* d_req, const int32_t* d_topk,
                          int32_t* d_row_ids, hs_stream_t stream) {
+  CallRange nvtx_range("hs_replay_topk");
   if (!p || group < 0 || group >= p->d.n_groups || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
@@ -440,6 +470,7 @@ hs_status hs_replay_topk(hs_pool* p, int32_t group, int32_t n, const int32_t* d_
 
 hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, int32_t n, const uint16_t* d_q, const int32_t* d_row_ids,
                                float sm_scale, uint16_t* d_out, float* d_lse, hs_stream_t stream) {
+  CallRange nvtx_range("hs_sparse_mla_decode");
   if (!p || layer < 0 || layer >= p->cfg.n_layers || n < 0 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
   if (n == 0) return HS_OK;
   if (!d_q || !d_row_ids || !d_out || !aligned16(d_q) || !aligned16(d_out)) return HS_ERR_INVALID;
@@ -455,6 +486,7 @@ hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, int32_t n, const uint1
 
 hs_status hs_offload_pages(hs_pool* p, int32_t n, const int32_t* d_pool_pages, const int64_t* d_host_pages,
                            hs_stream_t stream) {
+  CallRange nvtx_range("hs_offload_pages");
   if (!p || n < 0) return HS_ERR_INVALID;
   p->settled_rows = nullptr;
   if (n == 0) return HS_OK;
@@ -466,6 +498,7 @@ hs_status hs_offload_pages(hs_pool* p, int32_t n, const int32_t* d_pool_pages, c
 
 hs_status hs_link_probe(const void* h_mapped, int64_t n_host_rows, int32_t row_bytes, const int64_t* d_src_rows,
                         int64_t n, void* d_dst, hs_stream_t stream) {
+  CallRange nvtx_range("hs_link_probe");
   if (!h_mapped || !d_src_rows || !d_dst || n < 0 || n_host_rows < 1 || row_bytes < 16 || row_bytes % 16 ||
       !aligned16(d_dst) || !aligned16(h_mapped))
     return HS_ERR_INVALID;
@@ -481,7 +514,15 @@ hs_status hs_link_probe(const void* h_mapped, int64_t n_host_rows, int32_t row_b
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
+hs_status hs_wait_selftest(hs_pool* p, hs_stream_t stream) {
+  CallRange nvtx_range("hs_wait_selftest");
+  if (!p) return HS_ERR_INVALID;
+  wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p->d);
+  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
 hs_status hs_get_error(hs_pool* p, hs_status* device_status, hs_stream_t stream) {
+  CallRange nvtx_range("hs_get_error");
   if (!p || !device_status) return HS_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   HS_CUDA_TRY(cudaStreamSynchronize(st));
@@ -493,6 +534,7 @@ hs_status hs_get_error(hs_pool* p, hs_status* device_status, hs_stream_t stream)
 }
 
 hs_status hs_get_counters(hs_pool* p, hs_counters* out, int32_t reset, hs_stream_t stream) {
+  CallRange nvtx_range("hs_get_counters");
   if (!p || !out) return HS_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   HS_CUDA_TRY(cudaStreamSynchronize(st));

@@ -66,6 +66,7 @@ _SIGS = {
     "hs_get_error": [_P, ctypes.POINTER(ctypes.c_int), _P],
     "hs_get_counters": [_P, ctypes.POINTER(Counters), _I, _P],
     "hs_link_probe": [_P, ctypes.c_int64, _I, _P, ctypes.c_int64, _P, _P],
+    "hs_wait_selftest": [_P, _P],
 }
 
 
@@ -206,6 +207,10 @@ class Pool:
         v = ctypes.c_int(0)
         _check("hs_get_error", lib.hs_get_error(self.handle, ctypes.byref(v), _stream(stream)))
         return v.value
+
+    def wait_selftest(self, stream=None) -> None:
+        """hs_wait_selftest: a bounded device wait that runs out (HS_ERR_TIMEOUT)."""
+        _check("hs_wait_selftest", lib.hs_wait_selftest(self.handle, _stream(stream)))
 
     def raise_on_device_error(self, stream=None) -> None:
         st = self.get_error(stream)

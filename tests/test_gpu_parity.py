@@ -92,6 +92,9 @@ def test_parity_small_configs(name):
     ("small_batch", dict(topk=1152, hot_rows=5 * 1152, pressure=False)),
     # 1 query token x 9 row splits: 16 heads per CTA, merge through distributed shared memory
     ("small_single", dict(topk=1152, hot_rows=2 * 1152)),
+    # top-K 128: a single row split, no cluster and no merge (16 and 64 heads per CTA)
+    ("small_single", dict(topk=128, hot_rows=2 * 128)),
+    ("small_batch", dict(topk=128, hot_rows=5 * 128, pressure=False)),
 ])
 def test_parity_odd_split_count(name, over):
     cfg, wl, plans, oracle, gpu = _setup(name, **over)
