@@ -107,6 +107,23 @@ def test_parity_odd_split_count(name, over):
         gpu.close()
 
 
+@pytest.mark.parametrize("name,over", [
+    # 32 query heads (two head groups of 16 per token) and 48 index heads (N = 48 MMAs)
+    ("small_single", dict(n_heads=32, n_idx_heads=48)),
+    # 32 query heads and 32 index heads with 4 MTP tokens per request
+    ("small_batch", dict(n_heads=32, n_idx_heads=32)),
+])
+def test_parity_other_head_counts(name, over):
+    cfg, wl, plans, oracle, gpu = _setup(name, **over)
+    try:
+        for plan in plans:
+            o = oracle.step(plan)
+            g = gpu.step(plan)
+            check_step(cfg, wl, plan, o, g, gpu, oracle)
+    finally:
+        gpu.close()
+
+
 def test_parity_tiny_all_pages_resident_no_misses():
     cfg, wl, plans, oracle, gpu = _setup("tiny", host_only_frac=0.0)
     try:
