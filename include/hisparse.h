@@ -251,7 +251,9 @@ hs_status hs_replay_topk(hs_pool* pool, int32_t group, int32_t n_tokens, const i
  * (512 dequantised latent + 64 rope) of each selected row, o = softmax(z) . v_t
  * over the 512 latent dims, lse = log sum exp z.
  *  d_q [n, H, 576] bf16, 16-byte aligned; d_row_ids [n, K] (-1 skipped);
- *  d_out [n, H, 512] bf16, 16-byte aligned; d_lse nullable [n, H] fp32.
+ *  d_out [n, H, 512] bf16, 16-byte aligned; d_lse nullable [n, H] fp32. d_out
+ *  may also be pinned, mapped host memory (the kernel then writes the output over
+ *  the host link itself, with no copy afterwards).
  *  Per-group FP8 scales must be below 256 (HS_ERR_INVALID for misaligned
  *  pointers or out-of-range arguments).
  *  Layers of one selection: when the previous launch of this pool was
