@@ -601,14 +601,7 @@ template <int HPC>
 static hs_status launch_attention_hpc(hs_pool* p, int layer, int n, int n_splits, const uint16_t* d_q,
                                       const int32_t* d_rows, float scale_log2, uint16_t* d_out, float* d_lse,
                                       bool settled, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attention_kernel<HPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             AtPlan<HPC>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(attention_kernel<HPC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return HS_ERR_CUDA;
-    attr = true;
-  }
+  if (ensure_kernel_attrs(attention_kernel<HPC>, AtPlan<HPC>::SMEM, true) != HS_OK) return HS_ERR_CUDA;
   const int n_hgrp = p->cfg.n_heads / HPC;
   return launch_pdl(attention_kernel<HPC>, dim3(n_splits, n * n_hgrp, 1), dim3(AT_THREADS, 1, 1), AtPlan<HPC>::SMEM,
                     st, n_splits, p->d, layer, d_q, d_rows, scale_log2, d_out, d_lse, settled ? 1 : 0);

@@ -27,6 +27,10 @@
 // each CTA then emits its selected tokens in ascending order at its offset.
 #include <cooperative_groups.h>
 
+#include <atomic>
+#include <map>
+#include <mutex>
+
 #include "hs_select.cuh"
 
 namespace cg = cooperative_groups;
@@ -803,15 +807,38 @@ select_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* 
   cluster_sync();   // peers may still read this CTA's shared memory until here
 }
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
+int num_sms() {   // of the current device, looked up once per device
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDev) dev = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (n <= 0) n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
   return n;
+}
+
+hs_status ensure_kernel_attrs(const void* kernel, int smem, bool nonportable_cluster) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;   // (kernel, device) -> limit set
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kernel, dev);
+  const auto it = done.find(key);
+  if (it != done.end() && it->second >= smem) return HS_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      (nonportable_cluster && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                                  cudaSuccess)) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  done[key] = smem;
+  return HS_OK;
 }
 
 hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const int32_t* d_limit,
@@ -820,12 +847,7 @@ hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const 
   const int n_max = ((p->cfg.max_q_per_req * p->cfg.n_idx_heads) + 15) & ~15;
   const IxLayout L = ix_layout(n_max, p->cfg.max_tokens, d_hist0 != nullptr);
   if (L.stages < 2) return HS_ERR_INVALID;
-  static int attr_smem = 0;
-  if (attr_smem < L.smem) {
-    if (cudaFuncSetAttribute(indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem) != cudaSuccess)
-      return HS_ERR_CUDA;
-    attr_smem = L.smem;
-  }
+  if (ensure_kernel_attrs(indexer_kernel, L.smem) != HS_OK) return HS_ERR_CUDA;
   return launch_pdl(indexer_kernel, dim3(num_sms()), dim3(IX_THREADS), L.smem, st, 0, p->d, il, n, d_req, d_limit,
                     d_q, d_w, d_scores, p->cfg.max_ctx, L, d_hist0);
 }
@@ -833,14 +855,7 @@ hs_status launch_indexer(hs_pool* p, int il, int n, const int32_t* d_req, const 
 template <int CL>
 hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
                            int32_t* d_topk, bool fp_keys, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(select_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_SMEM) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(select_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return HS_ERR_CUDA;
-    attr = true;
-  }
+  if (ensure_kernel_attrs(select_kernel<CL>, SEL_SMEM, CL > 8) != HS_OK) return HS_ERR_CUDA;
   return launch_pdl(select_kernel<CL>, dim3(n * CL), dim3(SEL_THREADS), SEL_SMEM, st, CL, p->d, scores, ld, d_limit,
                     d_topk, fp_keys ? 1 : 0);
 }

@@ -406,12 +406,7 @@ hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, co
   // alternate tiles go to alternate epilogue warpgroups: an even accumulator count
   // keeps every accumulator with one warpgroup, so its phase waits never alias
   if (L.stages < 2 || L.n_acc % F8_EPI_GROUPS || il < 0 || il >= (int)p->idx_tmaps.size()) return HS_ERR_INVALID;
-  static int attr_smem = 0;
-  if (attr_smem < L.smem) {
-    if (cudaFuncSetAttribute(indexer_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem) != cudaSuccess)
-      return HS_ERR_CUDA;
-    attr_smem = L.smem;
-  }
+  if (ensure_kernel_attrs(indexer_fp8_kernel, L.smem) != HS_OK) return HS_ERR_CUDA;
   return launch_pdl(indexer_fp8_kernel, dim3(num_sms()), dim3(F8_THREADS), L.smem, st, 0, p->d, p->idx_tmaps[il],
                     il, n, d_req, d_limit, d_q, d_w, reinterpret_cast<long long*>(d_keys), d_scores,
                     p->cfg.max_ctx, L, d_hist0);

@@ -414,6 +414,16 @@ inline hs_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   return launch_pdl_cluster(kernel, grid, block, smem, st, dim3(cluster_x > 0 ? cluster_x : 1, 1, 1), args...);
 }
 
+// ---- kernel attributes, set once per (kernel, device) -------------------------------
+// Raises `kernel`'s dynamic shared-memory limit to at least `smem` bytes (and allows
+// cluster sizes above 8 when asked) on the current device, once per device: the
+// attributes are per device, and a process may drive pools on several GPUs.
+hs_status ensure_kernel_attrs(const void* kernel, int smem, bool nonportable_cluster);
+template <typename... KArgs>
+inline hs_status ensure_kernel_attrs(void (*kernel)(KArgs...), int smem, bool nonportable_cluster = false) {
+  return ensure_kernel_attrs(reinterpret_cast<const void*>(kernel), smem, nonportable_cluster);
+}
+
 // ---- host-side launch helpers (defined in hs_pool.cu) ----------------------------
 // d_hist0: nullable; the selection's level-0 histogram sums, which the scoring
 // kernel fills when the selection runs wide for one query token (select_hist0)

@@ -466,12 +466,7 @@ constexpr int RS_SMEM = RS_MAXU * (4 + 4 + 4 + 1 + 8);
 
 hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* d_req, const int32_t* d_topk,
                          int32_t* d_row_ids, hs_plan_entry* d_plan, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RS_SMEM) != cudaSuccess)
-      return HS_ERR_CUDA;
-    attr = true;
-  }
+  if (ensure_kernel_attrs(resolve_kernel, RS_SMEM) != HS_OK) return HS_ERR_CUDA;
   // one cluster of RS_COPY_CTAS CTAs per token (the first token of each request resolves it)
   return launch_pdl_cluster(resolve_kernel, dim3(n, RS_COPY_CTAS), dim3(RS_THREADS), RS_SMEM, st,
                             dim3(1, RS_COPY_CTAS, 1), p->d, group, step, n, d_req, d_topk, d_row_ids, d_plan);

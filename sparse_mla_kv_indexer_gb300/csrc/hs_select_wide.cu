@@ -334,13 +334,7 @@ hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, c
                              int32_t* d_topk, bool fp_keys, int G, bool hist0_done, cudaStream_t st) {
   if (G < 1 || G > SW_MAX_G || n < 1 || n > p->d.sel_ws_tokens || n * G > num_sms() || (hist0_done && n != 1))
     return HS_ERR_INVALID;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(select_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SW_SMEM) !=
-        cudaSuccess)
-      return HS_ERR_CUDA;
-    attr = true;
-  }
+  if (ensure_kernel_attrs(select_wide_kernel, SW_SMEM) != HS_OK) return HS_ERR_CUDA;
   return launch_pdl(select_wide_kernel, dim3(n * G), dim3(SW_THREADS), SW_SMEM, st, 0, p->d, scores, ld, d_limit,
                     d_topk, fp_keys ? 1 : 0, G, hist0_done ? 1 : 0);
 }
