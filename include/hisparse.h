@@ -58,9 +58,11 @@
 extern "C" {
 #endif
 
-/* Longest context a pool accepts (tokens per request). The top-K selection splits a
- * query token's scores over 16 CTAs and keeps a 2-byte bucket per score of its share
- * in shared memory, which bounds the share at 81,920 scores. */
+/* Longest context a pool accepts (tokens per request). With many query tokens the
+ * top-K selection splits a token's scores over a 16-CTA cluster and keeps a 2-byte
+ * bucket per score of its share in shared memory, which bounds the share at 81,920
+ * scores. (With few query tokens the selection spreads each token over up to one CTA
+ * per SM, holding at most 12,288 scores per CTA.) */
 #define HS_MAX_CTX 1310720
 
 typedef struct CUstream_st* hs_stream_t; /* a cudaStream_t; NULL = legacy default stream */
