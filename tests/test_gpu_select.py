@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 
 from oracle import indexer as OI
+from sparse_mla_kv_indexer_gb300 import workload as W
 
 pytestmark = pytest.mark.gpu
 
@@ -100,6 +101,96 @@ def test_selection_matches_full_sort(kind):
                     for i in range(n_tok):
                         assert np.array_equal(got[i], want[i]), (kind, n_tok, entry, i)
             if kind == "equal":
+                for i in range(n_tok):   # all scores tie: the K lowest token ids
+                    m = min(K, limits[i])
+                    assert np.array_equal(want[i][:m], np.arange(m)), i
+    finally:
+        pool.close()
+
+
+# ---- FP8 keys (128 e4m3 values and an fp32 scale per key) ------------------------
+#
+# Every key value, query value and head weight is a small integer (e4m3 holds the
+# integers up to 16 exactly) and every scale a power of two, so each score
+# (|sum_d q k| <= 128 * 64 per head, 16 heads, |w| <= 16, below 2^24) is exact in
+# fp32 whatever the order of the sums: the scores and the top-K must equal the fp64
+# oracle's exactly, ties included. All queries zero makes every head product a
+# signed zero (-0 where a key value is negative); the score of such a token is 0
+# and ties with the +0 scores.
+
+def _fp8_keys(kind, rng):
+    if kind == "equal":
+        k = np.broadcast_to(rng.integers(1, 9, size=128).astype(np.float32), (CTX, 128))
+        scale = np.ones(CTX, np.float32)
+    elif kind == "three":
+        base = rng.integers(-8, 9, size=(3, 128)).astype(np.float32)
+        k = base[rng.integers(0, 3, size=CTX)]
+        scale = np.ones(CTX, np.float32)
+    else:   # "zero" and "random": mixed signs, scales 1/2, 1 or 2
+        k = rng.integers(-8, 9, size=(CTX, 128)).astype(np.float32)
+        scale = np.float32(2.0) ** rng.integers(-1, 2, size=CTX).astype(np.float32)
+    return W.encode_e4m3(np.ascontiguousarray(k)), scale.astype(np.float32)
+
+
+def _fp8_queries(kind, n_tok, rng):
+    if kind == "zero":
+        q = np.zeros((n_tok, HI, 128), np.float32)
+    else:
+        q = rng.integers(-8, 9, size=(n_tok, HI, 128)).astype(np.float32)
+        if kind == "equal":
+            q = np.abs(q)
+    w = rng.integers(1, 17, size=(n_tok, HI)).astype(np.float32)
+    if kind == "random":
+        w *= np.where(rng.random((n_tok, HI)) < 0.25, -1.0, 1.0).astype(np.float32)   # negative scores too
+    return W.encode_e4m3(q), w
+
+
+def _fp8_pages(codes, scale):
+    n = codes.shape[0] // 64
+    page = np.empty((n, 64 * 128 + 64 * 4), np.uint8)
+    page[:, :64 * 128] = codes.reshape(n, 64 * 128)
+    page[:, 64 * 128:] = scale.astype("<f4").view(np.uint8).reshape(n, 64 * 4)
+    return page.reshape(-1)
+
+
+@pytest.mark.parametrize("kind", ["equal", "zero", "three", "random"])
+def test_fp8_selection_matches_full_sort(kind):
+    torch = _torch()
+    from sparse_mla_kv_indexer_gb300 import hisparse as H
+    rng = np.random.default_rng({"equal": 11, "zero": 12, "three": 13, "random": 14}[kind])
+    codes, scale = _fp8_keys(kind, rng)
+    pages = CTX // 64
+    pc = H.PoolConfig(page_size=64, row_bytes=656, idx_dim=128, n_idx_heads=HI, n_heads=16, topk=K,
+                      n_layers=1, layers_per_indexer=1, num_pages=4, num_idx_pages=pages, max_requests=2,
+                      max_ctx=CTX, max_q_per_req=4, hot_rows=4096, max_tokens=8, idx_format=H.IDX_FP8,
+                      host_pages=1)
+    kv = [torch.zeros(4 * 64 * 656, dtype=torch.uint8, device="cuda")]
+    ix = [torch.from_numpy(_fp8_pages(codes, scale)).to("cuda")]
+    host = torch.zeros(64 * 656, dtype=torch.uint8, pin_memory=True)
+    pool = H.Pool(pc, kv, ix, host)
+    try:
+        for r in range(2):
+            pool.set_pages(r, 0, idx_pages=list(range(pages)))
+        for reqs, limits in BATCHES:
+            n_tok = len(reqs)
+            qc, w = _fp8_queries(kind, n_tok, rng)
+            so = [OI.scores_fp8(qc[i], w[i], codes[:limits[i]], scale[:limits[i]]) for i in range(n_tok)]
+            want = np.stack([OI.topk_real(s, K) for s in so])
+            d_req = torch.tensor(reqs, dtype=torch.int32, device="cuda")
+            d_lim = torch.tensor(limits, dtype=torch.int32, device="cuda")
+            d_q = torch.from_numpy(qc.reshape(n_tok, -1)).to("cuda")
+            d_w = torch.from_numpy(w).to("cuda")
+            out = torch.full((n_tok, K), -7, dtype=torch.int32, device="cuda")
+            sc = torch.full((n_tok, CTX), float("nan"), dtype=torch.float32, device="cuda")
+            for _ in range(2):   # the wide selection clears its scratch for the next call
+                pool.indexer_topk_fp8(0, d_req, d_lim, d_q, d_w, out, sc)
+                torch.cuda.synchronize()
+                assert pool.get_error() == 0, (kind, n_tok)
+                got, gs = out.cpu().numpy(), sc.cpu().numpy()
+                for i in range(n_tok):
+                    assert np.array_equal(gs[i, :limits[i]].astype(np.float64), so[i]), (kind, n_tok, i)
+                    assert np.array_equal(got[i], want[i]), (kind, n_tok, i)
+            if kind in ("equal", "zero"):
                 for i in range(n_tok):   # all scores tie: the K lowest token ids
                     m = min(K, limits[i])
                     assert np.array_equal(want[i][:m], np.arange(m)), i
