@@ -97,20 +97,20 @@ typedef struct hs_pool_config {
   int32_t page_size;          /* tokens per page; must be 64 */
   int32_t row_bytes;          /* bytes per KV row; must be 656 ([P2] footnote 1, fp8_ds_mla) */
   int32_t idx_dim;            /* index key dims; must be 128 */
-  int32_t n_idx_heads;        /* H_i, 1..64 */
+  int32_t n_idx_heads;        /* H_i: 16, 32, 48 or 64 */
   int32_t n_heads;            /* attention heads H: 16, 32 or 64 */
   int32_t topk;               /* K: multiple of 128, 128..2048 */
   int32_t n_layers;           /* sparse-MLA layers, 1..64 */
   int32_t layers_per_indexer; /* IndexShare group size ([P1] "Sparsity when you need it"), 1..8 */
-  int32_t num_pages;          /* pool pages in each layer's KV tensor */
-  int32_t num_idx_pages;      /* pages in each indexer layer's key cache */
+  int32_t num_pages;          /* pool pages in each layer's KV tensor, >= 1, num_pages * 64 < 2^31 */
+  int32_t num_idx_pages;      /* pages in each indexer layer's key cache, >= 1 */
   int32_t max_requests;       /* request slots */
   int32_t max_ctx;            /* max positions per request, multiple of 128, <= HS_MAX_CTX */
   int32_t max_q_per_req;      /* query tokens per request per call, 1..4 */
-  int32_t hot_rows;           /* hot-buffer capacity per (request, group), multiple of 64 */
+  int32_t hot_rows;           /* hot-buffer capacity per (request, group), multiple of 64, 64..16384 */
   int32_t max_tokens;         /* query tokens per call, 1..1024 */
   int32_t idx_format;         /* index-key format: HS_IDX_INT8 or HS_IDX_FP8 */
-  int64_t host_pages;         /* pages in the pinned host pool */
+  int64_t host_pages;         /* pages in the pinned host pool, >= 1 */
 } hs_pool_config;
 
 /* One resolved selection ([P1] "How it works": resident / hot / miss). */
@@ -159,7 +159,9 @@ hs_status hs_pool_destroy(hs_pool* pool);
 
 /* ---------------------------------------------------------------------------
  * Host-side residency updates, issued between steps (stream-ordered copies of
- * small host arrays; the host arrays may be reused as soon as the call returns).
+ * small host arrays, which the call takes by value: the arrays, page-locked or
+ * not, may be reused as soon as the call returns; those copies from pageable host
+ * memory make hs_request_set_pages and hs_hot_lease not graph-capturable).
  * ------------------------------------------------------------------------- */
 
 /* Set n consecutive logical pages [first_page, first_page + n) of request req.

@@ -177,6 +177,24 @@ __global__ void wait_selftest_kernel(Dev D) {
   }
 }
 
+// The residency calls copy small host arrays to the device in stream order, each
+// through a pageable buffer on this stack rather than from the caller's array: the
+// runtime stages a pageable source before cudaMemcpyAsync returns, so the caller may
+// reuse its arrays at once even when they are page-locked (whose copies would
+// otherwise read them later, in stream order). No heap memory is allocated.
+template <typename T>
+cudaError_t copy_staged(T* d_dst, const T* h_src, int n, cudaStream_t st) {
+  constexpr int CHUNK = 4096 / sizeof(T);
+  T buf[CHUNK];
+  for (int i = 0; i < n; i += CHUNK) {
+    const int m = n - i < CHUNK ? n - i : CHUNK;
+    std::memcpy(buf, h_src + i, sizeof(T) * m);
+    const cudaError_t e = cudaMemcpyAsync(d_dst + i, buf, sizeof(T) * m, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 int launch_blocks(long long work, int threads) {
   long long b = (work + threads - 1) / threads;
   long long cap = 4ll * num_sms();
@@ -357,12 +375,9 @@ hs_status hs_request_set_pages(hs_pool* p, int32_t req, int32_t first_page, int3
     if (h_idx_pages && (h_idx_pages[i] < -1 || h_idx_pages[i] >= p->cfg.num_idx_pages)) return HS_ERR_INVALID;
     if (h_host_pages && (h_host_pages[i] < -1 || h_host_pages[i] >= p->cfg.host_pages)) return HS_ERR_INVALID;
   }
-  if (h_block_table)
-    HS_CUDA_TRY(cudaMemcpyAsync(p->d.bt + off, h_block_table, sizeof(int32_t) * n, cudaMemcpyHostToDevice, st));
-  if (h_idx_pages)
-    HS_CUDA_TRY(cudaMemcpyAsync(p->d.idx_bt + off, h_idx_pages, sizeof(int32_t) * n, cudaMemcpyHostToDevice, st));
-  if (h_host_pages)
-    HS_CUDA_TRY(cudaMemcpyAsync(p->d.host_pg + off, h_host_pages, sizeof(int64_t) * n, cudaMemcpyHostToDevice, st));
+  if (h_block_table) HS_CUDA_TRY(copy_staged(p->d.bt + off, h_block_table, n, st));
+  if (h_idx_pages) HS_CUDA_TRY(copy_staged(p->d.idx_bt + off, h_idx_pages, n, st));
+  if (h_host_pages) HS_CUDA_TRY(copy_staged(p->d.host_pg + off, h_host_pages, n, st));
   return HS_OK;
 }
 
@@ -380,11 +395,9 @@ hs_status hs_hot_lease(hs_pool* p, int32_t req, int32_t group, int32_t n, const 
     if (h_pool_pages[i] < 0 || h_pool_pages[i] >= p->cfg.num_pages) return HS_ERR_INVALID;
   if (n == 0) return HS_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  HS_CUDA_TRY(cudaMemcpyAsync(p->d.hot_pages + rg * p->d.hot_pages_max + cur, h_pool_pages, sizeof(int32_t) * n,
-                              cudaMemcpyHostToDevice, st));
+  HS_CUDA_TRY(copy_staged(p->d.hot_pages + rg * p->d.hot_pages_max + cur, h_pool_pages, n, st));
   p->n_hot_host[rg] = cur + n;
   HS_CUDA_TRY(cudaMemcpyAsync(p->d.n_hot + rg, &p->n_hot_host[rg], sizeof(int32_t), cudaMemcpyHostToDevice, st));
-  // the pageable source above is staged before return; keep the mirror stable until then
   return HS_OK;
 }
 
