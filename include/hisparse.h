@@ -231,7 +231,9 @@ hs_status hs_indexer_topk(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
  * the least recently used slot (stamp, then slot, ascending; empty slots first)
  * and copies that token's row of every layer of the group from the pinned host
  * pool into it. step must increase from call to call for a given (req, group).
- *  d_topk [n, K] from hs_indexer_topk; d_row_ids [n, K] out (-1 for pads);
+ *  d_topk [n, K] as hs_indexer_topk writes it: each row ascending, -1 pads at
+ *  the end (ids >= max_ctx set HS_ERR_BAD_ID and count as pads); d_row_ids [n, K]
+ *  out (-1 for pads);
  *  d_plan nullable [n, K] out. */
 hs_status hs_resolve_topk(hs_pool* pool, int32_t group, int32_t step, int32_t n_tokens,
                           const int32_t* d_req, const int32_t* d_topk, int32_t* d_row_ids,

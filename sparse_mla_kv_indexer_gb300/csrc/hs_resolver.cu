@@ -9,8 +9,9 @@
 // decision. With MTP the verification tokens of a request resolve together.
 //
 // One CTA per request segment (the tokens of one request in the batch):
-//   1. U = ascending union of the segment's selected tokens (bitonic sort +
-//      dedup in shared memory; a single token's top-K is already ascending);
+//   1. U = ascending union of the segment's selected tokens: each token's top-K is
+//      ascending, so the rows are merged by rank (binary searches, one pass) and
+//      repeats dropped; a single row is taken as it is;
 //   2. classify each t in U: block table >= 0 -> RESIDENT; hot slot -> HIT
 //      (stamp = step); else MISS;
 //   3. victims = leased slots not hit this step, ordered by (stamp, slot): a
@@ -96,7 +97,7 @@ resolve_kernel(Dev D, int group, int step, int n_tok, const int32_t* __restrict_
   // miss's copy record (pool row, token)
   unsigned long long* V = reinterpret_cast<unsigned long long*>(kind + RS_MAXU);
   __shared__ int wt[32];
-  __shared__ int s_tot, s_cnt[3], s_bin, s_before, s_min, s_listed;
+  __shared__ int s_tot, s_cnt[3], s_bin, s_before, s_min, s_listed, s_len[4];
   __shared__ uint32_t hbin[RS_HBINS];
   __shared__ int32_t s_hotp[256];                                   // hot pages of (request, group)
 
@@ -165,32 +166,74 @@ resolve_kernel(Dev D, int group, int step, int n_tok, const int32_t* __restrict_
         __syncthreads();
         nU = s_tot;     // pads are at the end of an ascending top-K row
       } else {
+        // T rows of K entries, pads (and ids beyond the context) as INT_MAX
         int np = 1;
         while (np < n_in) np <<= 1;
+        if (tid < 4) s_len[tid] = 0;
         for (int i = tid; i < np; i += RS_THREADS) {
           int t = i < n_in ? topk[(size_t)b * K + i] : -1;
           if (t >= D.max_ctx) { set_status(D.status, HS_ERR_BAD_ID); t = -1; }
           U[i] = t < 0 ? INT_MAX : t;
+          info[i] = INT_MAX;
         }
         __syncthreads();
-        bitonic_sort(U, np);
-        // dedup, keep order
+        // A top-K row is ascending with its pads at the end; each row's length is the
+        // index of its first pad. Rows of that form are merged by rank; any other
+        // input is sorted whole.
+        int bad_row = 0;
+        for (int i = tid; i < n_in; i += RS_THREADS) {
+          const int k = i % K;
+          const bool last = k == K - 1 || U[i + 1] == INT_MAX;
+          if (k != K - 1 && U[i + 1] != INT_MAX && U[i] >= U[i + 1]) bad_row = 1;
+          if (U[i] != INT_MAX && last) s_len[i / K] = k + 1;
+        }
+        const bool by_rank = !__syncthreads_or(bad_row);
+        if (by_rank) {
+          // An entry's place in the merged order is its index in its own row plus the
+          // entries of the other rows before it: those < t, and those == t of earlier
+          // rows (equal tokens keep row order, so every place is taken once).
+          for (int i = tid; i < n_in; i += RS_THREADS) {
+            const int j = i / K, k = i - j * K;
+            if (k >= s_len[j]) continue;
+            const int t = U[i];
+            int pos = k;
+            for (int o = 0; o < T; ++o) {
+              if (o == j) continue;
+              const int32_t* row = U + o * K;
+              int lo = 0, hi = s_len[o];   // first entry > t (earlier rows) or >= t (later rows)
+              while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (o < j ? row[mid] <= t : row[mid] < t) lo = mid + 1; else hi = mid;
+              }
+              pos += lo;
+            }
+            info[pos] = t;
+          }
+        } else {
+          bitonic_sort(U, np);
+        }
+        __syncthreads();
+        // drop repeats of the ascending sequence, keep the order
+        const int32_t* srt = by_rank ? info : U;
+        int32_t* dst = by_rank ? U : info;
         constexpr int IPT = RS_MAXU / RS_THREADS;
         int f[IPT], cnt = 0;
 #pragma unroll
         for (int k = 0; k < IPT; ++k) {
           int i = tid * IPT + k;
-          f[k] = (i < np && U[i] != INT_MAX && (i == 0 || U[i] != U[i - 1])) ? 1 : 0;
+          f[k] = (i < np && srt[i] != INT_MAX && (i == 0 || srt[i] != srt[i - 1])) ? 1 : 0;
           cnt += f[k];
         }
         int pos = rs_block_scan(cnt, wt, &s_tot);
 #pragma unroll
         for (int k = 0; k < IPT; ++k)
-          if (f[k]) info[pos++] = U[tid * IPT + k];
+          if (f[k]) dst[pos++] = srt[tid * IPT + k];
         __syncthreads();
         nU = s_tot;
-        for (int i = tid; i < nU; i += RS_THREADS) U[i] = info[i];
-        __syncthreads();
+        if (!by_rank) {
+          for (int i = tid; i < nU; i += RS_THREADS) U[i] = info[i];
+          __syncthreads();
+        }
       }
 
       // ---- 2. classify: block-table and token->slot entries of all of a thread's
