@@ -133,6 +133,11 @@ typedef struct hs_counters {
 
 typedef struct hs_pool hs_pool;
 
+/* Check a pool geometry without touching the GPU: HS_OK if hs_pool_init would
+ * accept it (the limits listed in hs_pool_config), HS_ERR_INVALID otherwise (or
+ * for a NULL cfg). hs_pool_init applies the same check first. */
+hs_status hs_pool_config_check(const hs_pool_config* cfg);
+
 /*
  * Create a pool over caller-owned memory.
  *  cfg         geometry (copied).

@@ -254,11 +254,8 @@ static hs_status make_key_tensor_maps(hs_pool* p, void* const* d_idx_layers) {
   return HS_OK;
 }
 
-hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void* const* d_idx_layers,
-                       void* h_host_kv, hs_pool** out) {
-  CallRange nvtx_range("hs_pool_init");
-  if (!cfg || !d_kv_layers || !d_idx_layers || !h_host_kv || !out) return HS_ERR_INVALID;
-  *out = nullptr;
+hs_status hs_pool_config_check(const hs_pool_config* cfg) {
+  if (!cfg) return HS_ERR_INVALID;
   const hs_pool_config& c = *cfg;
   if (c.page_size != PAGE || c.row_bytes != ROW || c.idx_dim != IDX_DIM) return HS_ERR_INVALID;
   if (c.n_idx_heads < 16 || c.n_idx_heads > 64 || c.n_idx_heads % 16) return HS_ERR_INVALID;
@@ -274,6 +271,16 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
   if (c.hot_rows < PAGE || c.hot_rows % PAGE || c.hot_rows > 16384) return HS_ERR_INVALID;
   if (c.max_tokens < 1 || c.max_tokens > 1024 || c.host_pages < 1) return HS_ERR_INVALID;
   if (c.idx_format != HS_IDX_INT8 && c.idx_format != HS_IDX_FP8) return HS_ERR_INVALID;
+  return HS_OK;
+}
+
+hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void* const* d_idx_layers,
+                       void* h_host_kv, hs_pool** out) {
+  CallRange nvtx_range("hs_pool_init");
+  if (!cfg || !d_kv_layers || !d_idx_layers || !h_host_kv || !out) return HS_ERR_INVALID;
+  *out = nullptr;
+  if (hs_pool_config_check(cfg) != HS_OK) return HS_ERR_INVALID;
+  const hs_pool_config& c = *cfg;
   const int n_groups = (c.n_layers + c.layers_per_indexer - 1) / c.layers_per_indexer;
   for (int l = 0; l < c.n_layers; ++l)
     if (!d_kv_layers[l] || !aligned16(d_kv_layers[l])) return HS_ERR_INVALID;

@@ -50,6 +50,7 @@ class Counters(ctypes.Structure):
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
 _SIGS = {
+    "hs_pool_config_check": [ctypes.POINTER(PoolConfig)],
     "hs_pool_init": [ctypes.POINTER(PoolConfig), ctypes.POINTER(_P), ctypes.POINTER(_P), _P, ctypes.POINTER(_P)],
     "hs_pool_destroy": [_P],
     "hs_request_set_pages": [_P, _I, _I, _I, _P, _P, _P, _P],
@@ -113,6 +114,11 @@ def _host_array(values, ctype):
         return None
     arr = (ctype * len(values))(*[int(v) for v in values])
     return ctypes.cast(arr, _P), arr
+
+
+def config_ok(cfg: PoolConfig) -> bool:
+    """hs_pool_config_check: whether hs_pool_init would accept this geometry (no GPU needed)."""
+    return lib.hs_pool_config_check(ctypes.byref(cfg)) == 0
 
 
 def link_probe(host_rows, row_bytes: int, src_rows, dst, stream=None) -> None:

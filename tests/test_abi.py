@@ -67,10 +67,19 @@ def test_bad_geometry_is_invalid(lib):
     out = ctypes.c_void_p()
     for key, bad in [("page_size", 32), ("row_bytes", 640), ("idx_dim", 64), ("n_heads", 48),
                      ("topk", 100), ("topk", 4096), ("max_ctx", 1000), ("hot_rows", 100),
-                     ("max_q_per_req", 5), ("max_tokens", 0), ("n_idx_heads", 8)]:
+                     ("max_q_per_req", 5), ("max_tokens", 0), ("n_idx_heads", 8), ("n_idx_heads", 24),
+                     ("n_idx_heads", 80), ("hot_rows", 16384 + 64), ("num_pages", 1 << 25), ("num_idx_pages", 0),
+                     ("host_pages", 0), ("max_ctx", 1310720 + 128), ("n_layers", 65), ("layers_per_indexer", 9),
+                     ("idx_format", 2), ("max_tokens", 1025)]:
         cfg = PoolConfig(**{**good, key: bad})
+        assert lib.hs_pool_config_check(ctypes.byref(cfg)) == 1, key
         assert lib.hs_pool_init(ctypes.byref(cfg), ptrs, ptrs, ctypes.c_void_p(16), ctypes.byref(out)) == 1, key
+    for key, ok in [("n_idx_heads", 16), ("n_idx_heads", 48), ("n_heads", 16), ("topk", 128), ("max_q_per_req", 4),
+                    ("hot_rows", 16384), ("max_ctx", 1310720), ("idx_format", 1), ("layers_per_indexer", 8)]:
+        assert lib.hs_pool_config_check(ctypes.byref(PoolConfig(**{**good, key: ok}))) == 0, key
+    assert lib.hs_pool_config_check(None) == 1
     cfg = PoolConfig(**good)
+    assert lib.hs_pool_config_check(ctypes.byref(cfg)) == 0
     misaligned = (ctypes.c_void_p * 8)(*([24] * 8))
     assert lib.hs_pool_init(ctypes.byref(cfg), misaligned, ptrs, ctypes.c_void_p(16), ctypes.byref(out)) == 1
 
