@@ -23,7 +23,8 @@
  *   the caller and must outlive the pool. The library owns only the opaque
  *   hs_pool and its device metadata, allocated by hs_pool_init and freed by
  *   hs_pool_destroy. No call between hs_pool_init and hs_pool_destroy
- *   allocates device or host memory.
+ *   allocates device memory or page-locked host memory (the first launch of each
+ *   kernel on a device only records its attributes in a small host-side table).
  * - Hot-path calls (hs_append_rows .. hs_offload_pages) are asynchronous on the
  *   given stream, do not synchronise with the host and read no device data on
  *   the host, so a sequence of them can be captured in a CUDA graph. Errors the
