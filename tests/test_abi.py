@@ -92,3 +92,17 @@ def test_binding_constants_match_the_header():
     assert H.MAX_CTX % 128 == 0 and H.MAX_CTX < (1 << 21)   # token ids fit the 21-bit tie-break field
     for code, name in H.STATUS.items():
         assert re.search(rf"\b{name}\s*=\s*{code}\b", text), name
+
+
+@pytest.mark.parametrize("name", ["tiny", "ctx128k", "batch32", "ctx1m", "multiturn", "small_single", "small_batch",
+                                  "small_groups", "small_reuse", "short_ctx", "tiny_fp8", "ctx128k_fp8", "ctx1m_fp8",
+                                  "small_batch_fp8"])
+def test_every_workload_geometry_is_accepted(lib, name):
+    """The pool each workload builds passes hs_pool_config_check, so no shape fails
+    only at hs_pool_init on the GPU."""
+    from sparse_mla_kv_indexer_gb300 import schedule as S
+    from sparse_mla_kv_indexer_gb300 import workload as W
+    from sparse_mla_kv_indexer_gb300.driver import pool_config
+    cfg = W.named_config(name)
+    pc = pool_config(W.Workload(cfg), S.Schedule(cfg).setup)
+    assert lib.hs_pool_config_check(ctypes.byref(pc)) == 0
