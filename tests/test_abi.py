@@ -106,3 +106,42 @@ def test_every_workload_geometry_is_accepted(lib, name):
     cfg = W.named_config(name)
     pc = pool_config(W.Workload(cfg), S.Schedule(cfg).setup)
     assert lib.hs_pool_config_check(ctypes.byref(pc)) == 0
+
+
+def test_a_c_program_builds_and_calls_the_library(lib, tmp_path):
+    """The header is plain C (C99, no C++ needed): a C program includes it, links
+    libhisparse.so, and calls the host-only entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    from sparse_mla_kv_indexer_gb300 import build
+    src = tmp_path / "abi_check.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "hisparse.h"
+int main(void) {
+  hs_pool_config c;
+  memset(&c, 0, sizeof c);
+  c.page_size = 64; c.row_bytes = 656; c.idx_dim = 128; c.n_idx_heads = 64; c.n_heads = 64;
+  c.topk = 2048; c.n_layers = 4; c.layers_per_indexer = 4; c.num_pages = 100; c.num_idx_pages = 100;
+  c.max_requests = 1; c.max_ctx = 131072; c.max_q_per_req = 1; c.hot_rows = 4096; c.max_tokens = 1;
+  c.idx_format = HS_IDX_INT8; c.host_pages = 10;
+  if (hs_pool_config_check(&c) != HS_OK) return 1;
+  c.topk = 100;
+  if (hs_pool_config_check(&c) != HS_ERR_INVALID) return 2;
+  if (strcmp(hs_status_string(HS_ERR_CAPACITY), "hot buffer capacity exceeded") != 0) return 3;
+  if (hs_sparse_mla_decode(NULL, 0, 1, NULL, NULL, 1.0f, NULL, NULL, NULL) != HS_ERR_INVALID) return 4;
+  printf("ok\n");
+  return 0;
+}
+''')
+    exe = tmp_path / "abi_check"
+    lib_dir = os.path.dirname(build.LIB)
+    name = os.path.basename(build.LIB)[3:-3]          # libhisparse.so -> hisparse
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I" + os.path.join(ROOT, "include"), str(src),
+                    "-L" + lib_dir, "-l" + name, "-Wl,-rpath," + lib_dir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
