@@ -49,6 +49,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle's CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-call-timing", action="store_true", help="skip the single-call graph timings")
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="workloads timed after the headline one on a single GPU, reported under 'workloads' "
+                         "(empty: none)")
+    ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each extra workload")
     return ap.parse_args()
 
 
@@ -252,11 +256,12 @@ def algorithmic_bytes(cfg, plans, counters_misses_rows):
             per_req[t.req] = max(per_req.get(t.req, 0), t.limit)
         keys += sum(per_req.values())
     keys /= len(plans)
-    n_tok = len(plans[0].tokens)
+    n_tok = sum(len(p.tokens) for p in plans) / len(plans)
+    n_app = n_tok + sum(hi - lo for p in plans for (_, lo, hi) in p.tick.prefill) / len(plans)
     idx = keys * (132 if cfg.idx_fp8 else 128)
     attn = n_tok * (cfg.topk * 660 + cfg.n_heads * 2176)
     offl = sum(len(p.offload) for p in plans) / len(plans) * 64 * 656 * cfg.n_layers
-    append = n_tok * (cfg.n_layers * 656 + cfg.n_groups * 128) * 2
+    append = n_app * (cfg.n_layers * 656 + cfg.n_groups * 128) * 2
     return {"indexer_topk": idx, "sparse_mla_decode": attn, "offload_pages": offl, "append": append,
             "resolve_topk": counters_misses_rows * 656 + n_tok * cfg.topk * 8}
 
@@ -369,13 +374,16 @@ def time_calls(torch, sess, i, flush, stream, reps=20):
     plan, host, d = sess.steps[i]
     pool = sess.run.pool
     g0, l0 = 0, cfg.group_layers(0)[0]
+    n = sess.tokens(i)
+    ch = sess.run.append_chunk()
+    topk, rows, o_l0 = sess.topk[g0][:n], sess.row_ids[g0][:n], sess.out[l0][:n]
     fns = {
-        "append": lambda: pool.append_rows(d["req"], d["pos"], d["kv_rows"], d["idx_keys"]),
+        "append": lambda: pool.append_rows(d["app_req"][:ch], d["app_pos"][:ch], d["kv_rows"][:ch], d["idx_keys"][:ch]),
         "indexer_topk": lambda: sess.run.indexer_topk(g0, d["req"], d["limit"], d["q_idx"][g0], d["w_idx"][g0],
-                                                      sess.topk[g0]),
-        "resolve_topk": lambda: pool.resolve_topk(g0, plan.step, d["req"], sess.topk[g0], sess.row_ids[g0]),
-        "sparse_mla_decode": lambda: pool.sparse_mla_decode(l0, d["q_attn"][l0], sess.row_ids[g0],
-                                                            sess.run.wl.sm_scale(), sess.out[l0]),
+                                                      topk),
+        "resolve_topk": lambda: pool.resolve_topk(g0, plan.step, d["req"], topk, rows),
+        "sparse_mla_decode": lambda: pool.sparse_mla_decode(l0, d["q_attn"][l0], rows,
+                                                            sess.run.wl.sm_scale(), o_l0),
     }
     if len(plan.offload):
         fns["offload_pages"] = lambda: pool.offload_pages(d["off_pool"], d["off_host"])
@@ -470,29 +478,23 @@ def reference_arm(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
-def main():
-    args = parse_args()
-    rank, world, local = dist_setup(args.gpus)
-    if args.impl == "reference":
-        rc = reference_arm(args, rank, world)
-        barrier(world)
-        return rc
+def measure(args, name, K, Wm, rank, world, local, cpu_baseline):
+    """Time `name` on this GPU: K graph-replayed steps after Wm warm-up steps,
+    device-resident and end to end; returns the JSON object of the bench line."""
     import torch
-    from sparse_mla_kv_indexer_gb300 import build as B
-    if rank == 0 or not os.path.exists(B.LIB):
-        B.build()
-    barrier(world)
     from sparse_mla_kv_indexer_gb300 import schedule as S
     from sparse_mla_kv_indexer_gb300 import workload as W
     from sparse_mla_kv_indexer_gb300.driver import BenchSession, GpuRun
 
-    torch.cuda.set_device(local)
-    K, Wm = args.steps, max(3, args.warmup)
     total = 2 * (Wm + K)
-    cfg = workload_config(args.workload, total, rank)
+    cfg = workload_config(name, total, rank)
     wl = W.Workload(cfg)
     sch = S.Schedule(cfg)
-    plans = [sch.plan(s) for s in range(total)]
+    plans, occupancy = [], []
+    for s in range(total):
+        plans.append(sch.plan(s))
+        hot = sum(len(v) for v in sch.hot_of.values())
+        occupancy.append((int((sch.bt >= 0).sum()), hot, len(sch.free)))
     run = GpuRun(wl, sch.setup)
     dev_sess = BenchSession(run, plans[:Wm + K], mode="device")
     host_sess = BenchSession(run, plans[Wm + K:], mode="host")
@@ -532,7 +534,7 @@ def main():
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     t_total = sum(step_ms) / 1000.0
     t_max = max_over_ranks(t_total, world)
-    tokens = dev_sess.n_tokens * K
+    tokens = sum(dev_sess.tokens(i) for i in range(Wm, Wm + K))
     tokens_all = sum_over_ranks(tokens, world)
     value = tokens_all / t_max
 
@@ -559,20 +561,22 @@ def main():
     run.pool.raise_on_device_error()
     del hgraphs
     e2e_t = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1000.0, world)
-    e2e_value = sum_over_ranks(host_sess.n_tokens * K, world) / e2e_t
+    e2e_value = sum_over_ranks(sum(host_sess.tokens(i) for i in range(Wm, Wm + K)), world) / e2e_t
 
     if rank != 0:
-        barrier(world)
-        return 0
+        run.close()
+        return None
 
     # ---- roofline of the dominant call ----
+    timed_plans = plans[Wm:Wm + K]
     miss_rows = counters.h2d_bytes / 656.0 / K
-    alg = algorithmic_bytes(cfg, plans[Wm:Wm + K], miss_rows)
+    alg = algorithmic_bytes(cfg, timed_plans, miss_rows)
     share = {k: v["ms"] * v["per_step"] for k, v in calls.items()} or {"sparse_mla_decode": 0.0}
     dom = max(share, key=share.get)
     avg_ms = calls[dom]["ms"] if calls else 0.0
     peak, peak_kind = measured_peaks()
-    dom_bytes = alg.get(dom, 0.0)
+    # the single-call graph times step Wm + K - 1: its own algorithmic bytes
+    dom_bytes = algorithmic_bytes(cfg, [plans[Wm + K - 1]], miss_rows).get(dom, 0.0) if calls else alg.get(dom, 0.0)
     achieved = dom_bytes / (avg_ms / 1000.0) / 1e9 if avg_ms > 0 else 0.0
     tkey = dom + "_fp8" if dom == "indexer_topk" and cfg.idx_fp8 else dom   # key of the committed traffic
     step_bytes = alg["indexer_topk"] * cfg.n_groups + alg["sparse_mla_decode"] * cfg.n_layers
@@ -583,7 +587,7 @@ def main():
     from sparse_mla_kv_indexer_gb300 import hisparse as HS
     link = host_link_probe(torch, HS)
     miss_bytes = counters.h2d_bytes / K
-    n_tok = len(plans[Wm].tokens)
+    n_tok = sum(len(p.tokens) for p in timed_plans) / len(timed_plans)
     keys_scored = alg["indexer_topk"] / (132 if cfg.idx_fp8 else 128)
     flops = (n_tok * cfg.n_layers * cfg.topk * cfg.n_heads * 2176.0 +
              keys_scored * cfg.n_groups * cfg.t_q * 2.0 * 128 * cfg.n_idx_heads)
@@ -593,20 +597,23 @@ def main():
     roof_step_s = max(t_mem, t_tensor)
 
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        v, sample, cores = oracle_sample(args.workload, args.cpu_seconds)
+    if cpu_baseline and world == 1:
+        v, sample, cores = oracle_sample(name, args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+    occ = occupancy[Wm:Wm + K]
+    ended = sum(len(p.tick.releases) for p in plans[:Wm + K])
+    turn_inputs = sum(len(p.tick.prefill) for p in timed_plans)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": 1000.0 * t_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8->int64 (indexer, exact), fp8-e4m3/bf16->fp32 (attention)",
         "data": "synthetic",
-        "config": config_line(args.workload, cfg),
+        "config": config_line(name, cfg),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes,
-                     "traffic": ncu_traffic(KERNEL_FILES.get(tkey, []), tkey, args.workload)},
+                     "traffic": ncu_traffic(KERNEL_FILES.get(tkey, []), tkey, name)},
         "step_roofline": {"algorithmic_hbm_bytes": step_bytes, "miss_bytes": miss_bytes,
                           "host_link_gbs": link["single_row_gbs"], "tensor_flops": flops,
                           "tensor_peak_tflops": tflops, "tensor_peak_source": tflops_kind,
@@ -623,6 +630,11 @@ def main():
                      "miss_link_us_per_step": miss_bytes / (link["single_row_gbs"] * 1e9) * 1e6,
                      "resolve_us_per_step": (calls["resolve_topk"]["ms"] * calls["resolve_topk"]["per_step"] * 1e3
                                              if "resolve_topk" in calls else None)},
+        "pool_pages": {"total": run.setup.num_pages,
+                       "block_table_mean": statistics.mean(o[0] for o in occ),
+                       "hot_mean": statistics.mean(o[1] for o in occ),
+                       "free_min": min(o[2] for o in occ),
+                       "requests_ended_by_last_timed_step": ended, "turn_inputs_written_in_timed_steps": turn_inputs},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": statistics.mean(host_sess.h2d_bytes),
                 "d2h_bytes_per_step": host_sess.d2h_bytes},
         "gpu_launches": launches,
@@ -630,7 +642,42 @@ def main():
         "clocks": clk,
         "cpu_baseline": cpu,
     }
-    print(json.dumps(line), flush=True)
+    run.close()
+    del run, dev_sess, host_sess, flush
+    torch.cuda.empty_cache()
+    return line
+
+
+# workloads timed beside the headline in a default single-GPU run (the second target
+# workload of the method, 1M context, and the two batched shapes), each with fewer steps
+EXTRA_WORKLOADS = ("ctx1m", "batch32", "multiturn")
+EXTRA_KEYS = ("value", "ms_per_step", "steps", "warmup", "roofline", "step_roofline", "resolver", "pool_pages",
+              "e2e", "gpu_launches", "clocks", "config", "breakdown_ms_per_call", "calls_per_step")
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        rc = reference_arm(args, rank, world)
+        barrier(world)
+        return rc
+    import torch
+    from sparse_mla_kv_indexer_gb300 import build as B
+    if rank == 0 or not os.path.exists(B.LIB):
+        B.build()
+    barrier(world)
+    torch.cuda.set_device(local)
+    K, Wm = args.steps, max(3, args.warmup)
+    line = measure(args, args.workload, K, Wm, rank, world, local, not args.no_cpu_baseline)
+    extras = [w for w in (args.extra.split(",") if args.extra else []) if w and w != args.workload]
+    if world == 1 and extras:
+        line["workloads"] = {}
+        for w in extras:
+            sub = measure(args, w, min(K, args.extra_steps), Wm, rank, world, local, False)
+            line["workloads"][w] = {k: sub[k] for k in EXTRA_KEYS}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     barrier(world)
     return 0
 

@@ -2,8 +2,11 @@
 
 One step, per "vLLM Part 1" (sections "How it works" and the proactive copy
 paragraph) and "vLLM Part 2" (IndexShare, MQA-form sparse MLA):
-  0. apply the host tick (block-table changes, hot leases) from the schedule;
-  1. append the step's new KV rows (every sparse layer) and index keys;
+  0. apply the host tick from the schedule: block-table changes, the hot buffers
+     of requests that ended emptied (their pages go back to the pool; "Offload
+     only where needed": hot pages are returned when not needed), hot leases;
+  1. append the step's new KV rows (every sparse layer) and index keys: the input
+     positions of a turn that begins this step, then the step's query tokens;
   2. per indexer group: scores + top-K for every query token, then the
      resolver for every request, then sparse MLA for every layer of the group;
   3. copy the pages this step completed, all layers, to their host pages.
@@ -67,9 +70,9 @@ class OracleRun:
         for (r, g, pages) in tick.leases:
             self.hot[(r, g)].lease(pages)
 
-    def append(self, tokens):
-        for tk in tokens:
-            r, pos = tk.req, tk.pos
+    def append(self, positions):
+        """Write the KV row (every layer) and index keys of each (request, position)."""
+        for r, pos in positions:
             p, off = pos // PAGE, pos % PAGE
             row = int(self.bt[r, p]) * PAGE + off
             assert self.bt[r, p] >= 0
@@ -90,7 +93,8 @@ class OracleRun:
     def step(self, plan) -> Dict[str, object]:
         cfg, wl, s = self.cfg, self.wl, plan.step
         self.apply_tick(plan.tick)
-        self.append(plan.tokens)
+        self.append([(r, pos) for (r, lo, hi) in plan.tick.prefill for pos in range(lo, hi)])
+        self.append([(t.req, t.pos) for t in plan.tokens])
         toks = plan.tokens
         n = len(toks)
         K = cfg.topk

@@ -36,6 +36,13 @@ def pool_config(wl: Workload, setup: Setup) -> H.PoolConfig:
         idx_format=H.IDX_FP8 if cfg.idx_fp8 else H.IDX_INT8, host_pages=setup.host_pages)
 
 
+def _stack(items, shape=None, dtype=None) -> np.ndarray:
+    """np.stack, or an empty [0, *shape] array when a step has no query tokens."""
+    if items or shape is None:
+        return np.stack(items)
+    return np.zeros((0,) + tuple(shape), dtype)
+
+
 class GpuRun:
     def __init__(self, wl: Workload, setup: Setup, keep_scores: bool = False, device: str = "cuda"):
         import torch
@@ -93,31 +100,52 @@ class GpuRun:
 
     # ------------------------------------------------------------------
     def apply_tick(self, tick) -> None:
-        for (r, p, pg) in tick.bt_set:
-            self.pool.set_pages(r, p, block_table=[pg])
+        # runs of consecutive pages of one request go in one call (a request that ends
+        # turns its whole block table into placeholders)
+        i, bt = 0, tick.bt_set
+        while i < len(bt):
+            r, p0, _ = bt[i]
+            j = i + 1
+            while j < len(bt) and bt[j][0] == r and bt[j][1] == p0 + (j - i):
+                j += 1
+            self.pool.set_pages(r, p0, block_table=[e[2] for e in bt[i:j]])
+            i = j
         for r in tick.releases:
             self.pool.hot_release(r)
         for (r, g, pages) in tick.leases:
             self.pool.hot_lease(r, g, pages)
+
+    def append_chunk(self) -> int:
+        """Positions per hs_append_rows call: at most max_tokens, a multiple of 4 so that
+        every chunk of 132-byte FP8 key records starts 16-byte aligned."""
+        mt = self.pc.max_tokens
+        return mt if mt < 4 else mt - mt % 4
 
     def step_inputs(self, plan: StepPlan) -> Dict[str, np.ndarray]:
         """Host arrays of one step, in batch order (tokens grouped by request)."""
         cfg, wl, s = self.cfg, self.wl, plan.step
         toks = plan.tokens
         t_q = cfg.t_q
+        # positions written this step: a beginning turn's input, then the query tokens
+        app = [(r, pos) for (r, lo, hi) in plan.tick.prefill for pos in range(lo, hi)] + [(t.req, t.pos) for t in toks]
+        assert not plan.tick.prefill or self.append_chunk() % 4 == 0
         out = {
             "req": np.array([t.req for t in toks], np.int32),
-            "pos": np.array([t.pos for t in toks], np.int32),
             "limit": np.array([t.limit for t in toks], np.int32),
-            "kv_rows": np.stack([np.stack([wl.kv_rows(t.req, l)[t.pos] for l in range(cfg.n_layers)]) for t in toks]),
-            "idx_keys": np.stack([np.stack([self._key_record(t.req, g, t.pos) for g in range(cfg.n_groups)])
-                                  for t in toks]),
-            "q_idx": np.stack([np.stack([self._idx_query(t.req, g, s)[0][i % t_q] for i, t in enumerate(toks)])
-                               for g in range(cfg.n_groups)]),
-            "w_idx": np.stack([np.stack([self._idx_query(t.req, g, s)[1][i % t_q] for i, t in enumerate(toks)])
-                               for g in range(cfg.n_groups)]),
-            "q_attn": np.stack([np.stack([wl.attn_queries(t.req, l, s)[i % t_q] for i, t in enumerate(toks)])
-                                for l in range(cfg.n_layers)]),
+            "app_req": np.array([a[0] for a in app], np.int32),
+            "app_pos": np.array([a[1] for a in app], np.int32),
+            "kv_rows": np.stack([np.stack([wl.kv_rows(r, l)[pos] for l in range(cfg.n_layers)]) for r, pos in app]),
+            "idx_keys": np.stack([np.stack([self._key_record(r, g, pos) for g in range(cfg.n_groups)])
+                                  for r, pos in app]),
+            "q_idx": _stack([_stack([self._idx_query(t.req, g, s)[0][i % t_q] for i, t in enumerate(toks)],
+                                    (cfg.n_idx_heads, IDX_DIM), np.uint8 if cfg.idx_fp8 else np.int8)
+                             for g in range(cfg.n_groups)]),
+            "w_idx": _stack([_stack([self._idx_query(t.req, g, s)[1][i % t_q] for i, t in enumerate(toks)],
+                                    (cfg.n_idx_heads,), np.float32 if cfg.idx_fp8 else np.int8)
+                             for g in range(cfg.n_groups)]),
+            "q_attn": _stack([_stack([wl.attn_queries(t.req, l, s)[i % t_q] for i, t in enumerate(toks)],
+                                     (cfg.n_heads, 576), np.uint16)
+                              for l in range(cfg.n_layers)]),
             "off_pool": np.array([o[2] for o in plan.offload], np.int32),
             "off_host": np.array([o[3] for o in plan.offload], np.int64),
         }
@@ -141,7 +169,12 @@ class GpuRun:
         else:
             self.pool.indexer_topk(g, req, limit, q, w, topk, scores)
 
-    def step(self, plan: StepPlan, collect: bool = True) -> Dict[str, object]:
+    def step(self, plan: StepPlan, collect: bool = True, topk_in=None) -> Dict[str, object]:
+        """One decode step through the C ABI. topk_in: optional per-group [n, K] host
+        arrays that the resolver and attention take instead of the indexer's own
+        selection (the indexer still runs; its selection is returned as "topk_own"),
+        so that two runs whose selections differ only at a near-tie stay in the same
+        residency state."""
         torch = self.torch
         cfg, dev = self.cfg, self.dev
         self.apply_tick(plan.tick)
@@ -149,10 +182,20 @@ class GpuRun:
         n = len(plan.tokens)
         K = cfg.topk
         req = torch.from_numpy(x["req"]).to(dev)
-        pos = torch.from_numpy(x["pos"]).to(dev)
         limit = torch.from_numpy(x["limit"]).to(dev)
-        self.pool.append_rows(req, pos, torch.from_numpy(x["kv_rows"]).to(dev),
-                              torch.from_numpy(x["idx_keys"]).to(dev))
+        a_req, a_pos = torch.from_numpy(x["app_req"]).to(dev), torch.from_numpy(x["app_pos"]).to(dev)
+        a_kv, a_ik = torch.from_numpy(x["kv_rows"]).to(dev), torch.from_numpy(x["idx_keys"]).to(dev)
+        ch = self.append_chunk()
+        for lo in range(0, a_req.numel(), ch):
+            self.pool.append_rows(a_req[lo:lo + ch], a_pos[lo:lo + ch], a_kv[lo:lo + ch], a_ik[lo:lo + ch])
+        if n == 0:     # every request has ended
+            res = {"topk": [np.zeros((0, K), np.int32)] * cfg.n_groups, "row_ids": [np.zeros((0, K), np.int32)] * cfg.n_groups,
+                   "plan": [np.zeros((0, K, PLAN_FIELDS), np.int32)] * cfg.n_groups, "scores": [None] * cfg.n_groups,
+                   "o": [np.zeros((0, cfg.n_heads, 512))] * cfg.n_layers, "lse": [np.zeros((0, cfg.n_heads))] * cfg.n_layers}
+            if len(plan.offload):
+                self.pool.offload_pages(torch.from_numpy(x["off_pool"]).to(dev), torch.from_numpy(x["off_host"]).to(dev))
+            res["status"] = self.pool.get_error()
+            return res
         res = {"topk": [], "row_ids": [], "plan": [], "scores": [], "o": [None] * cfg.n_layers,
                "lse": [None] * cfg.n_layers}
         for g in range(cfg.n_groups):
@@ -162,6 +205,9 @@ class GpuRun:
             sdt = torch.float32 if cfg.idx_fp8 else torch.int64
             scores = torch.empty((n, self.max_ctx), dtype=sdt, device=dev) if self.keep_scores else None
             self.indexer_topk(g, req, limit, q, w, topk, scores)
+            if topk_in is not None:
+                res.setdefault("topk_own", []).append(topk.cpu().numpy())
+                topk = torch.from_numpy(np.ascontiguousarray(topk_in[g], dtype=np.int32)).to(dev)
             row_ids = torch.empty((n, K), dtype=torch.int32, device=dev)
             plan_t = torch.empty((n, K, PLAN_FIELDS), dtype=torch.int32, device=dev)
             self.pool.resolve_topk(g, plan.step, req, topk, row_ids, plan_t)
@@ -207,6 +253,8 @@ class BenchSession:
     which moves many megabytes faster than the kernels' scattered writes over the link.
     (Splitting the input copy over a side stream to overlap it with the selection, or
     reading every input from host memory, measured slower.)
+    A step's query tokens are those of the requests still alive; a turn that begins
+    writes its input positions in the step's appends.
     """
 
     HOST_WRITE_MAX = 4 << 20
@@ -223,7 +271,7 @@ class BenchSession:
         for plan in plans:
             x = run.step_inputs(plan)
             arrays = {
-                "req": x["req"], "pos": x["pos"], "limit": x["limit"],
+                "req": x["req"], "limit": x["limit"], "app_req": x["app_req"], "app_pos": x["app_pos"],
                 "kv_rows": x["kv_rows"], "idx_keys": x["idx_keys"],
                 "q_idx": x["q_idx"], "w_idx": x["w_idx"],
                 "q_attn": x["q_attn"].view(np.int16),
@@ -235,8 +283,8 @@ class BenchSession:
                 for k, v in host.items():
                     offs[k] = total
                     total += (v.numel() * v.element_size() + 255) & ~255
-                pack = torch.empty(total, dtype=torch.uint8).pin_memory()
-                dpack = torch.empty(total, dtype=torch.uint8, device=dev)
+                pack = torch.empty(max(total, 256), dtype=torch.uint8).pin_memory()
+                dpack = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
                 devt = {}
                 for k, v in host.items():
                     nb = v.numel() * v.element_size()
@@ -247,6 +295,8 @@ class BenchSession:
                 devt = {k: v.to(dev) for k, v in host.items()}
             self.steps.append((plan, host, devt))
         n = cfg.n_requests * cfg.t_q
+        self.n_max = n
+        self.n_step = [len(p.tokens) for p in plans]
         self.n_tokens = n
         K = cfg.topk
         self.topk = [torch.empty((n, K), dtype=torch.int32, device=dev) for _ in range(cfg.n_groups)]
@@ -258,15 +308,28 @@ class BenchSession:
             self.out = self.out_host      # the attention writes its outputs into pinned host memory
         self.h2d_bytes = [h["_bytes"] if mode == "host" else sum(v.numel() * v.element_size() for v in h.values())
                           for _, h, _ in self.steps]
+        out_per_tok = cfg.n_layers * cfg.n_heads * 512 * 2
+        self.d2h_step = [nt * out_per_tok if mode == "host" else 0 for nt in self.n_step]
         self.d2h_bytes = self.out.numel() * self.out.element_size() if mode == "host" else 0
 
+    def tokens(self, i: int) -> int:
+        """Query tokens of step i (the requests alive at that step)."""
+        return self.n_step[i]
+
+    def appends(self, i: int) -> int:
+        """hs_append_rows calls of step i (turn inputs can need more than one)."""
+        n = self.steps[i][2]["app_req"].numel()
+        ch = self.run.append_chunk()
+        return -(-n // ch)
+
     def launches(self, i: int) -> int:
-        """Kernels one step launches: append; per indexer group the indexer, the
+        """Kernels one step launches: the appends; per indexer group the indexer, the
         select kernel and the resolver (which also copies its misses); one attention
         kernel per layer (the split merge runs inside it); offload when pages complete."""
         cfg = self.run.cfg
         plan = self.steps[i][0]
-        return 1 + cfg.n_groups * 3 + cfg.n_layers + (1 if len(plan.offload) else 0)
+        hot = cfg.n_groups * 3 + cfg.n_layers if self.n_step[i] else 0
+        return self.appends(i) + hot + (1 if len(plan.offload) else 0)
 
     def tick(self, i: int) -> None:
         self.run.apply_tick(self.steps[i][0].tick)
@@ -278,6 +341,7 @@ class BenchSession:
         run, cfg = self.run, self.run.cfg
         plan, host, d = self.steps[i]
         pool = run.pool
+        n = self.n_step[i]
 
         def timed(name, fn):
             if events is None:
@@ -292,14 +356,19 @@ class BenchSession:
         host_mode = self.mode == "host"
         if host_mode:
             host["_dpack"].copy_(host["_pack"], non_blocking=True)   # every input of the step, one copy
-        timed("append", lambda: pool.append_rows(d["req"], d["pos"], d["kv_rows"], d["idx_keys"]))
-        for g in range(cfg.n_groups):
-            timed("indexer_topk", lambda: run.indexer_topk(g, d["req"], d["limit"], d["q_idx"][g], d["w_idx"][g],
-                                                           self.topk[g]))
-            timed("resolve_topk", lambda: pool.resolve_topk(g, plan.step, d["req"], self.topk[g], self.row_ids[g]))
-            for l in cfg.group_layers(g):
-                timed("sparse_mla_decode", lambda: pool.sparse_mla_decode(l, d["q_attn"][l], self.row_ids[g],
-                                                                          run.wl.sm_scale(), self.out[l]))
+        ch = run.append_chunk()
+        for lo in range(0, d["app_req"].numel(), ch):
+            timed("append", lambda lo=lo: pool.append_rows(d["app_req"][lo:lo + ch], d["app_pos"][lo:lo + ch],
+                                                           d["kv_rows"][lo:lo + ch], d["idx_keys"][lo:lo + ch]))
+        if n:
+            for g in range(cfg.n_groups):
+                topk, rows = self.topk[g][:n], self.row_ids[g][:n]
+                timed("indexer_topk", lambda: run.indexer_topk(g, d["req"], d["limit"], d["q_idx"][g], d["w_idx"][g],
+                                                               topk))
+                timed("resolve_topk", lambda: pool.resolve_topk(g, plan.step, d["req"], topk, rows))
+                for l in cfg.group_layers(g):
+                    timed("sparse_mla_decode", lambda: pool.sparse_mla_decode(l, d["q_attn"][l], rows,
+                                                                              run.wl.sm_scale(), self.out[l][:n]))
         if len(plan.offload):
             timed("offload_pages", lambda: pool.offload_pages(d["off_pool"], d["off_host"]))
         if host_mode and not self.host_write:

@@ -23,6 +23,13 @@ this module fixes:
   requests start with placeholders for every complete page plus one hot page.
 * A page is queued for host materialisation in the step whose committed tokens
   complete it; all sparse layers of the page are copied together.
+* Multi-turn histories (the pages' OpenHands-style workload): a turn after the
+  first begins with its input positions written into the request's pages before
+  that step's decode tokens, like a prefill. When a request's history is done it
+  ends: its hot-buffer pages and every pool page of its block table (tail pages
+  included) return to the free list, its block-table entries become placeholders
+  and its hot buffers are emptied (section "Offload only where needed": hot pages
+  are leased on first need and returned when not needed).
 """
 from __future__ import annotations
 
@@ -47,7 +54,8 @@ class Tick:
     """Host actions applied before a step."""
     bt_set: List[Tuple[int, int, int]] = field(default_factory=list)      # (req, page, pool page or -1)
     leases: List[Tuple[int, int, List[int]]] = field(default_factory=list)  # (req, group, pool pages)
-    releases: List[int] = field(default_factory=list)
+    releases: List[int] = field(default_factory=list)                     # requests that ended
+    prefill: List[Tuple[int, int, int]] = field(default_factory=list)     # (req, first pos, end pos) written
 
 
 @dataclass
@@ -114,18 +122,23 @@ class Schedule:
         if self.pressure:
             num_pages = n_res + init_hot + cfg.pool_slack_pages
         else:
-            grow = sum(-(-(cfg.steps * cfg.accept + cfg.t_q) // PAGE) + 1 for _ in range(R))
+            if cfg.turns:
+                grow = sum(-(-cfg.final_len(r) // PAGE) - self.prefix[r] // PAGE + 1 for r in range(R))
+            else:
+                grow = sum(-(-(cfg.steps * cfg.accept + cfg.t_q) // PAGE) + 1 for _ in range(R))
             num_pages = n_res + init_hot + R * cfg.n_groups * (cfg.hot_rows // PAGE) + grow + cfg.pool_slack_pages
         for i, (r, p) in enumerate(resident):
             bt[r, p] = i
         free = list(range(n_res, num_pages))
         leases = []
         self.leased = {(r, g): 0 for r in range(R) for g in range(cfg.n_groups)}
+        self.hot_of: Dict[Tuple[int, int], List[int]] = {k: [] for k in self.leased}
         for r in cfg.prefix_reuse:
             for g in range(cfg.n_groups):
                 pg = free.pop(0)
                 leases.append((r, g, [pg]))
                 self.leased[(r, g)] = 1
+                self.hot_of[(r, g)].append(pg)
         heapq.heapify(free)
         self.free = free
         self.setup = Setup(num_pages, npm, bt.copy(), hp, mat.copy(), ip, idx_next, host_next,
@@ -142,6 +155,8 @@ class Schedule:
                     self.evict_heap.append((-1, r, p))
         heapq.heapify(self.evict_heap)
         self.committed = list(self.prefix)
+        self.events = [cfg.events(r) for r in range(R)]
+        self.alive = [True] * R
         self.evictions = 0
 
     # ------------------------------------------------------------------
@@ -175,16 +190,44 @@ class Schedule:
         n = -(-end // PAGE)
         return bool((self.bt[r, :n] < 0).any())
 
+    def _end_request(self, r: int, tick: Tick) -> None:
+        """Request end: every pool page of r (block table and hot buffers) to the free list."""
+        self.alive[r] = False
+        tick.releases.append(r)
+        for p in np.nonzero(self.bt[r] >= 0)[0]:
+            heapq.heappush(self.free, int(self.bt[r, p]))
+            self.bt[r, p] = -1
+            tick.bt_set.append((r, int(p), -1))
+        for g in range(self.cfg.n_groups):
+            for pg in self.hot_of[(r, g)]:
+                heapq.heappush(self.free, pg)
+            self.hot_of[(r, g)] = []
+            self.leased[(r, g)] = 0
+
     def plan(self, s: int) -> StepPlan:
         cfg = self.cfg
         R = cfg.n_requests
         tick = Tick()
         self._deferred: List[Tuple[int, int, int]] = []
-        start = [self.committed[r] for r in range(R)]
-        end = [start[r] + cfg.t_q for r in range(R)]
-        # 1. pages that this step's tokens land in
+        # 0. requests whose history is done end; a new turn writes its input positions
+        live = []
+        lo = list(self.committed)
         for r in range(R):
-            for p in range(start[r] // PAGE, (end[r] - 1) // PAGE + 1):
+            if not self.alive[r]:
+                continue
+            if s >= len(self.events[r]):
+                self._end_request(r, tick)
+                continue
+            live.append(r)
+            inp = self.events[r][s][0]
+            if inp:
+                tick.prefill.append((r, self.committed[r], self.committed[r] + inp))
+                self.committed[r] += inp
+        start = [self.committed[r] for r in range(R)]
+        end = [start[r] + cfg.t_q if r in live else start[r] for r in range(R)]
+        # 1. pages that this step's positions (turn input and tokens) land in
+        for r in live:
+            for p in range(lo[r] // PAGE, (end[r] - 1) // PAGE + 1):
                 if self.bt[r, p] < 0:
                     pg = self._alloc(tick, end)
                     self.bt[r, p] = pg
@@ -196,7 +239,7 @@ class Schedule:
         changed = True
         while changed:
             changed = False
-            for r in range(R):
+            for r in live:
                 if not self._needs_hot(r, end[r]):
                     continue
                 for g in range(cfg.n_groups):
@@ -210,20 +253,21 @@ class Schedule:
                     pages = [self._alloc(tick, end) for _ in range(target - cur)]
                     changed = True
                     self.leased[(r, g)] = target
+                    self.hot_of[(r, g)].extend(pages)
                     tick.leases.append((r, g, pages))
         for item in self._deferred:
             heapq.heappush(self.evict_heap, item)
         # 3. tokens
         tokens = []
-        for r in range(R):
+        for r in live:
             for j in range(cfg.t_q):
                 pos = start[r] + j
                 tokens.append(Token(r, pos, pos + 1))
-        # 4. commit and offload what this step completes
+        # 4. commit and offload what this step completes (turn input included)
         offload = []
-        for r in range(R):
+        for r in live:
             newc = start[r] + cfg.accept
-            for p in range(start[r] // PAGE, newc // PAGE):
+            for p in range(lo[r] // PAGE, newc // PAGE):
                 if (p + 1) * PAGE <= newc and not self.mat[r, p]:
                     assert self.bt[r, p] >= 0, "a completing page is always resident"
                     offload.append((r, p, int(self.bt[r, p]), int(self.hp[r, p])))

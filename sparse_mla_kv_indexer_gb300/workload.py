@@ -83,6 +83,15 @@ class WorkloadConfig:
     pressure: bool = False            # pool holds only the setup residency + slack: growth evicts
     idx_fp8: bool = False             # index keys as 128 e4m3 values + an fp32 scale (132-byte record)
     seed: int = 0
+    # Multi-turn histories (0 turns: one open-ended decode). A request's history is
+    # `turns` turns of `turn_steps` decode steps each; every turn after the first
+    # starts by writing `turn_input` new input positions (written like a prefill, not
+    # decoded). `history_step[r]` is where request r stands in its history at step 0;
+    # a request whose history is done ends and leaves the batch.
+    turns: int = 0
+    turn_input: int = 0
+    turn_steps: int = 0
+    history_step: Tuple[int, ...] = ()
 
     @property
     def n_groups(self) -> int:
@@ -92,9 +101,29 @@ class WorkloadConfig:
         lo = g * self.layers_per_indexer
         return list(range(lo, min(self.n_layers, lo + self.layers_per_indexer)))
 
+    def events(self, r: int) -> List[Tuple[int, int]]:
+        """(turn-input positions written, decode positions committed) of request r at
+        each step of the run, while it lives: a request that ends stops early."""
+        if self.turns == 0:
+            return [(0, self.accept)] * self.steps
+        out = []
+        for s in range(self.steps):
+            h = self.history_step[r] + s
+            if h >= self.turns * self.turn_steps:
+                break
+            boundary = s > 0 and h % self.turn_steps == 0
+            out.append((self.turn_input if boundary else 0, self.accept))
+        return out
+
     def final_len(self, r: int) -> int:
         """Highest position written by the run, plus one."""
-        return self.ctx_len[r] - self.t_q + (self.steps - 1) * self.accept + self.t_q
+        committed = self.ctx_len[r] - self.t_q
+        end = committed
+        for inp, acc in self.events(r):
+            committed += inp
+            end = committed + self.t_q
+            committed += acc
+        return end
 
     def max_ctx(self) -> int:
         m = max(self.final_len(r) for r in range(self.n_requests))
@@ -110,6 +139,12 @@ def _loguniform_lengths(n: int, lo: int, hi: int, seed: int) -> Tuple[int, ...]:
     return tuple(int(x) for x in np.round(v))
 
 
+def _history_context(first: int, turn_input: int, turn_steps: int, accept: int, h: int) -> int:
+    """Committed positions of a multi-turn request after h decode steps of its history:
+    the first turn's input, the input of every later turn begun, accept per step."""
+    return first + (h // turn_steps) * turn_input + h * accept
+
+
 def named_config(name: str) -> WorkloadConfig:
     """The workloads of the method's decode path, by name.
 
@@ -117,7 +152,9 @@ def named_config(name: str) -> WorkloadConfig:
     ctx128k     1 request, L = 131,072, 64 heads, 4 layers / 1 indexer, K = 2,048
     batch32     32 requests, L log-uniform in [8K, 256K], MTP3 (4 query tokens, 3 accepted)
     ctx1m       1 request, L = 1,048,576, 8 layers / 2 indexers, only the last 16 pages resident
-    multiturn   64 requests at 74,160+ tokens, MTP3, 40 % pool, 25 % prefix-reuse requests
+    multiturn   64 requests with 13-turn histories (74,160 first-turn tokens, +753 input and
+                220 output tokens per turn), MTP3, 40 % pool, 25 % prefix-reuse requests;
+                requests end when their histories do
     The small_* variants keep every structural feature at sizes the oracle finishes in seconds.
     """
     if name == "tiny":
@@ -136,9 +173,17 @@ def named_config(name: str) -> WorkloadConfig:
                               steps=128, tail_pages=16, host_only_frac=1.0, hot_rows=4096,
                               n_clusters=32, drift_sigma=1.0, jump_prob=0.1)
     if name == "multiturn":
-        return WorkloadConfig(name, 5, 64, tuple([74160] * 64), steps=74, t_q=4, accept=3,
+        # 13-turn histories: a 74,160-token first turn, then +753 input tokens per turn;
+        # 220 output tokens per turn decoded at MTP3 (74 steps of 3 accepted tokens).
+        # The 48 ongoing requests stand at spread points of their histories, the 16
+        # prefix-reuse requests early in their first turn.
+        turn_steps, turns, first, inp = 74, 13, 74160, 753
+        hist = tuple((r * 131 + 17) % (turns * turn_steps) if r < 48 else (r * 7) % turn_steps for r in range(64))
+        ctx = tuple(_history_context(first, inp, turn_steps, 3, h) + 4 for h in hist)
+        return WorkloadConfig(name, 5, 64, ctx, steps=74, t_q=4, accept=3,
                               tail_pages=8, host_only_frac=0.6, hot_rows=(3 + 2) * 2048,
-                              n_clusters=32, prefix_reuse=tuple(range(48, 64)), pressure=True)
+                              n_clusters=32, prefix_reuse=tuple(range(48, 64)), pressure=True,
+                              turns=turns, turn_input=inp, turn_steps=turn_steps, history_step=hist)
     # Reduced variants used by parity tests: same structure, fewer tokens.
     if name == "small_single":
         return WorkloadConfig(name, 12, 1, (16384,), steps=6, tail_pages=8,
@@ -155,6 +200,23 @@ def named_config(name: str) -> WorkloadConfig:
         return WorkloadConfig(name, 15, 3, (6000, 7000, 6500), topk=512, steps=5, t_q=4, accept=3,
                               tail_pages=4, host_only_frac=0.4, hot_rows=(3 + 2) * 512,
                               n_clusters=8, prefix_reuse=(2,), pressure=True)
+    if name == "small_multiturn":
+        # 3-turn histories of 3 steps per turn and +100 input tokens per turn, so that
+        # 8 steps cross five turn boundaries and end three requests (their pages go back
+        # to the pool and are leased again by the others)
+        turn_steps, turns, inp = 3, 3, 100
+        hist = (0, 4, 7, 2)
+        first = (5000, 6000, 3000, 4000)
+        ctx = tuple(_history_context(first[r], inp, turn_steps, 3, hist[r]) + 4 for r in range(4))
+        return WorkloadConfig(name, 17, 4, ctx, topk=512, steps=8, t_q=4, accept=3, tail_pages=4,
+                              host_only_frac=0.5, hot_rows=(3 + 2) * 512, n_clusters=8, pool_slack_pages=64,
+                              prefix_reuse=(3,), pressure=True, turns=turns, turn_input=inp,
+                              turn_steps=turn_steps, history_step=hist)
+    if name == "small_mtp":
+        # 6 requests x 4 MTP tokens at top-K 2,048: enough query tokens for the
+        # one-CTA-per-token attention; the shortest context is below K (pads)
+        return WorkloadConfig(name, 18, 6, (1500, 2600, 4000, 5200, 7000, 9100), steps=4, t_q=4, accept=3,
+                              tail_pages=4, host_only_frac=0.5, hot_rows=(3 + 2) * 2048, n_clusters=8)
     if name.endswith("_fp8"):   # the same shape with FP8 index keys
         return dataclasses.replace(named_config(name[:-4]), name=name, idx_fp8=True)
     if name == "short_ctx":

@@ -68,3 +68,44 @@ def test_cli_prints_a_table(capsys):
     C.main(["--kv-gib", "50", "--contexts", "8192,1048576"])
     out = capsys.readouterr().out
     assert "crossover" in out and "1048576" in out
+
+
+@pytest.mark.parametrize("name", ["batch32", "multiturn"])
+def test_capacity_matches_measured_pool_occupancy(name):
+    """The capacity model against the pool pages the residency schedule actually holds
+    for the 32-request and the multi-turn shapes, step by step (host side: the
+    schedule is what the bench and the tests drive; no kernel runs here).
+
+    Once a hot buffer has had the steps it needs to fill, every request that reads
+    from the host holds exactly the model's HiSparse floor, its resident tail plus
+    its hot buffers; the rest of the pool is the surplus residency that pressure
+    eviction lets go of page by page. Pool pages are conserved, and the model's
+    HiSparse concurrency on the measured pool covers the requests the run carries."""
+    import dataclasses
+    cfg = dataclasses.replace(W.named_config(name), steps=8)
+    sch = S.Schedule(cfg)
+    layout = C.KVLayout(cfg.n_layers, cfg.n_groups)
+    policy = C.HiSparsePolicy(cfg.topk, cfg.hot_rows // cfg.topk, cfg.layers_per_indexer, cfg.tail_pages)
+    grow = -(-cfg.t_q * cfg.topk // C.PAGE)
+    fill = -(-policy.hot_pages() // grow)        # steps a hot buffer needs to reach its cap
+    checked = 0
+    for s in range(cfg.steps):
+        p = sch.plan(s)
+        used = int((sch.bt >= 0).sum()) + sum(len(v) for v in sch.hot_of.values())
+        assert used + len(sch.free) == sch.setup.num_pages
+        live = sorted(set(t.req for t in p.tokens))
+        for r in live:
+            end = max(t.pos for t in p.tokens if t.req == r) + 1
+            hot = sum(len(sch.hot_of[(r, g)]) for g in range(cfg.n_groups))
+            assert hot <= C.n_groups(layout, policy) * policy.hot_pages()
+            last = (end - 1) // C.PAGE
+            tail = [pg for pg in range(max(0, last - cfg.tail_pages + 1), last + 1)]
+            if r in cfg.prefix_reuse or s < fill or not (sch.bt[r, :last + 1] < 0).any():
+                continue
+            assert all(sch.bt[r, pg] >= 0 for pg in tail)
+            assert len(tail) + hot == C.hisparse_pool_pages_per_request(layout, policy, end), (s, r)
+            checked += 1
+        floor = max(C.hisparse_pool_pages_per_request(layout, policy, max(t.limit for t in p.tokens if t.req == r))
+                    for r in live)
+        assert sch.setup.num_pages // floor >= len(live)
+    assert checked > 0

@@ -20,9 +20,11 @@ ATOL = 1e-2
 REL_L2 = 5e-3
 
 
-@pytest.mark.parametrize("name,steps,scores", [("ctx128k", 2, True), ("ctx1m", 1, False),
+@pytest.mark.parametrize("name,steps,scores", [("ctx128k", 2, True), ("ctx1m", 16, False),
                                                ("batch32", 1, False), ("multiturn", 1, False)])
 def test_parity_full_size(name, steps, scores):
+    """ctx1m runs 16 steps, so that the query drift and the 10 % per-step cluster jumps
+    make the resolver copy rows from host memory in steady state (misses after step 0)."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -35,11 +37,14 @@ def test_parity_full_size(name, steps, scores):
     gpu = GpuRun(wl, sch.setup, keep_scores=scores)
     rng = np.random.default_rng(0)
     total_miss = 0
+    later_miss = 0
     try:
         for plan in plans:
             o = oracle.step(plan)
             g = gpu.step(plan)
             total_miss += sum(len(m) for m in o["misses"])
+            if plan.step > 0:
+                later_miss += sum(len(m) for m in o["misses"])
             assert g["status"] == 0, f"device status {g['status']}"
             toks = plan.tokens
             for grp in range(cfg.n_groups):
@@ -67,5 +72,7 @@ def test_parity_full_size(name, steps, scores):
                 rel = np.linalg.norm(d) / np.linalg.norm(o["o"][l])
                 assert err <= ATOL and rel <= REL_L2, (plan.step, l, err, rel)
         assert gpu.pool.counters().misses == total_miss
+        if name == "ctx1m":
+            assert later_miss > 0, "no row copied from host after the first step"
     finally:
         gpu.close()

@@ -68,7 +68,7 @@ def check_step(cfg, wl, plan, o, g, gpu, oracle, exact_scores=True):
 
 
 @pytest.mark.parametrize("name", ["tiny", "short_ctx", "small_single", "small_batch", "small_groups",
-                                  "small_reuse"])
+                                  "small_reuse", "small_mtp"])
 def test_parity_small_configs(name):
     cfg, wl, plans, oracle, gpu = _setup(name)
     try:
@@ -83,6 +83,32 @@ def test_parity_small_configs(name):
         c = gpu.pool.counters()
         assert c.misses == total_miss and total_miss > 0
         assert c.h2d_bytes == total_h2d
+    finally:
+        gpu.close()
+
+
+def test_parity_multiturn_turn_inputs_and_request_end():
+    """Multi-turn histories: turn inputs written between decode steps (hs_append_rows),
+    requests that end (hs_hot_release and their block tables cleared) and their pages
+    leased again by the others. Every step matches the oracle as above, and the whole
+    KV pool and index caches equal the oracle's byte for byte after every step."""
+    cfg, wl, plans, oracle, gpu = _setup("small_multiturn")
+    try:
+        ends = prefills = 0
+        for plan in plans:
+            o = oracle.step(plan)
+            g = gpu.step(plan)
+            check_step(cfg, wl, plan, o, g, gpu, oracle)
+            for l in range(cfg.n_layers):
+                assert np.array_equal(gpu.pool_rows(l), oracle.pool[l]), (plan.step, l)
+            for grp in range(cfg.n_groups):
+                got = gpu.idx[grp].cpu().numpy().reshape(oracle.idx[grp].shape)
+                assert np.array_equal(got, oracle.idx[grp].view(got.dtype)), (plan.step, grp)
+            ends += len(plan.tick.releases)
+            prefills += len(plan.tick.prefill)
+        assert ends == 3 and prefills == 5
+        c = gpu.pool.counters()
+        assert c.misses > 0 and c.d2h_bytes > 0
     finally:
         gpu.close()
 

@@ -36,8 +36,8 @@ def _run(name, **over):
         plans.append(p)
         out = o.step(p)
         outs.append(out)
-        # tail pages of every request are resident after the tick
-        for r in range(cfg.n_requests):
+        # tail pages of every live request are resident after the tick
+        for r in sorted(set(t.req for t in p.tokens)):
             end = max(t.pos for t in p.tokens if t.req == r) + 1
             last = (end - 1) // PAGE
             for pg in range(max(0, last - cfg.tail_pages + 1), last + 1):
@@ -50,7 +50,7 @@ def _run(name, **over):
 
 
 @pytest.mark.parametrize("name", ["tiny", "small_single", "small_batch", "small_groups",
-                                  "small_reuse", "short_ctx"])
+                                  "small_reuse", "short_ctx", "small_multiturn"])
 def test_run_invariants(name):
     total_miss = 0
     for cfg, wl, o, p, out in _run(name):
@@ -109,8 +109,11 @@ def test_hot_cap_rule_matches_pages():
         assert cfg.hot_rows == (cfg.t_q - 1 + 2) * cfg.topk
 
 
-def test_schedule_pool_pages_never_shared():
-    cfg = W.named_config("small_batch")
+@pytest.mark.parametrize("name", ["small_batch", "small_multiturn"])
+def test_schedule_pool_pages_never_shared(name):
+    """Every pool page has exactly one owner (a block-table entry, a hot buffer or the
+    free list) after every step, across evictions, request ends and re-leases."""
+    cfg = W.named_config(name)
     sch = S.Schedule(cfg)
     owner = {}
     for r in range(cfg.n_requests):
@@ -122,14 +125,60 @@ def test_schedule_pool_pages_never_shared():
         for pg in pages:
             assert pg not in owner
             owner[pg] = "hot"
-    hot_pages = set(pg for pg, k in owner.items() if k == "hot")
+    hot = {(r, g): list(pages) for (r, g, pages) in sch.setup.leases}
+    released_pages = set()
+    reused = 0
     for s in range(cfg.steps):
         p = sch.plan(s)
+        for r in p.tick.releases:            # the schedule's own record of a request end
+            for g in range(cfg.n_groups):
+                released_pages.update(hot.pop((r, g), []))
         for (r, g, pages) in p.tick.leases:
-            hot_pages.update(pages)
+            reused += len(released_pages & set(pages))
+            hot.setdefault((r, g), []).extend(pages)
+        hot_pages = [pg for v in hot.values() for pg in v]
+        assert sorted(hot_pages) == sorted(pg for v in sch.hot_of.values() for pg in v)
         live = [int(x) for x in sch.bt.ravel() if x >= 0]
-        assert len(live) == len(set(live))
-        assert not (set(live) & hot_pages)
-        assert not (set(sch.free) & (set(live) | hot_pages))
+        reused += len(released_pages & set(live))
+        assert len(live) == len(set(live)) and len(hot_pages) == len(set(hot_pages))
+        assert not (set(live) & set(hot_pages))
+        assert not (set(sch.free) & (set(live) | set(hot_pages)))
         assert len(set(live)) + len(hot_pages) + len(sch.free) == sch.setup.num_pages
+        for r in p.tick.releases:
+            assert (sch.bt[r] < 0).all() and all(not sch.hot_of[(r, g)] for g in range(cfg.n_groups))
     assert sch.evictions > 0
+    if cfg.turns:
+        assert released_pages and reused > 0, "pages of ended requests are leased again"
+
+
+def test_multiturn_schedule_crosses_turns_and_ends_requests():
+    """small_multiturn: turn inputs are written at the turn boundaries of each request's
+    history, and requests whose history is done end (release, no more tokens)."""
+    cfg = W.named_config("small_multiturn")
+    sch = S.Schedule(cfg)
+    prefills, ends, toks = [], [], []
+    for s in range(cfg.steps):
+        p = sch.plan(s)
+        prefills += [(s, r, hi - lo) for (r, lo, hi) in p.tick.prefill]
+        ends += [(s, r) for r in p.tick.releases]
+        toks.append(sorted(set(t.req for t in p.tokens)))
+        for (r, lo, hi) in p.tick.prefill:      # the turn's input lands right before its tokens
+            assert min(t.pos for t in p.tokens if t.req == r) == hi
+    assert all(n == cfg.turn_input for (_, _, n) in prefills)
+    # history steps (0, 4, 7, 2) with 3 steps per turn and 3 turns
+    assert sorted((s, r) for (s, r, _) in prefills) == [(1, 3), (2, 1), (3, 0), (4, 3), (6, 0)]
+    assert ends == [(2, 2), (5, 1), (7, 3)]
+    for (s, r) in ends:
+        assert all(r not in toks[t] for t in range(s, cfg.steps))
+
+
+def test_multiturn_config_matches_the_pages_shape():
+    """The full multi-turn shape: 64 requests, 13 turns (74,160 first-turn tokens, +753
+    input and 220 output tokens per turn at 3 per step), contexts 74K..86K, 25 %
+    prefix-reuse requests."""
+    cfg = W.named_config("multiturn")
+    assert cfg.n_requests == 64 and cfg.turns == 13 and cfg.turn_input == 753
+    assert cfg.turn_steps * cfg.accept >= 220 > (cfg.turn_steps - 1) * cfg.accept
+    assert len(cfg.prefix_reuse) == 16
+    assert 74160 <= min(cfg.ctx_len) - cfg.t_q and max(cfg.ctx_len) <= 74160 + 12 * 753 + 13 * 222 + cfg.t_q
+    assert all(h < cfg.turns * cfg.turn_steps for h in cfg.history_step)

@@ -221,6 +221,34 @@ def test_resolver_hand_worked_sequence():
         assert res.n_hit == st["n_hit"] and res.n_resident == st["n_resident"]
 
 
+def test_resolver_release_then_lease_again():
+    """Request end empties the hot buffer; a later lease starts from empty slots
+    (hand-worked fixture, tests/golden/resolver_release_hand.json)."""
+    g = _load("resolver_release_hand.json")
+    bt = np.array(g["block_table"], np.int32)
+    hot = resolver.HotState()
+    for act in g["actions"]:
+        if "lease" in act:
+            hot.lease(act["lease"])
+        elif act.get("release"):
+            hot.release()
+            assert hot.pages == [] and hot.tok2slot == {}
+        else:
+            sel = _sel(act["select"])
+            res = resolver.resolve(sel, bt, hot, act["step"])
+            pos = {int(t): i for i, t in enumerate(sel[0])}
+            for tok, (kind, slot, row, ev) in act["expect"].items():
+                i = pos[int(tok)]
+                got = [int(res.kind[0, i]), int(res.slot[0, i]), int(res.row_ids[0, i]), int(res.evicted[0, i])]
+                assert got == [kind, slot, row, ev], (act["step"], tok, got)
+            assert len(res.misses) == act["n_miss"]
+            assert res.n_hit == act["n_hit"] and res.n_resident == act["n_resident"]
+        if "slots" in act:
+            assert len(hot.stamp) == len(hot.slot_token) == act["slots"]
+        # no token holds a slot twice and every map entry points back at its token
+        assert all(hot.slot_token[v] == t for t, v in hot.tok2slot.items())
+
+
 def test_resolver_capacity_error():
     bt = np.array([-1, -1], np.int32)
     hot = resolver.HotState()

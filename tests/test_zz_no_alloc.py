@@ -40,8 +40,8 @@ def test_noalloc_matches_regular_on_two_calls_in_a_row():
             n, K = len(plan.tokens), cfg.topk
             req = torch.from_numpy(x["req"]).to(dev)
             limit = torch.from_numpy(x["limit"]).to(dev)
-            gpu.pool.append_rows(req, torch.from_numpy(x["pos"]).to(dev), torch.from_numpy(x["kv_rows"]).to(dev),
-                                 torch.from_numpy(x["idx_keys"]).to(dev))
+            gpu.pool.append_rows(torch.from_numpy(x["app_req"]).to(dev), torch.from_numpy(x["app_pos"]).to(dev),
+                                 torch.from_numpy(x["kv_rows"]).to(dev), torch.from_numpy(x["idx_keys"]).to(dev))
             for g in range(cfg.n_groups):
                 q = torch.from_numpy(np.ascontiguousarray(x["q_idx"][g])).to(dev)
                 w = torch.from_numpy(np.ascontiguousarray(x["w_idx"][g])).to(dev)
