@@ -79,7 +79,8 @@ typedef enum hs_status {
   HS_ERR_BAD_ID = 7,       /* device: a page, row or token id out of range */
   HS_ERR_BAD_WEIGHT = 8,   /* device: a negative index-head weight */
   HS_ERR_SCRATCH_LIMIT = 9, /* request larger than the fixed scratch of hs_indexer_topk_noalloc */
-  HS_ERR_NOT_RESOLVED = 10  /* hs_replay_topk met a token that is neither resident nor hot */
+  HS_ERR_NOT_RESOLVED = 10, /* hs_replay_topk met a token that is neither resident nor hot */
+  HS_ERR_RANGE = 11         /* device: an attention input beyond the fp16 range of the batched path */
 } hs_status;
 
 /* Index-key formats.
@@ -212,7 +213,19 @@ hs_status hs_append_rows(hs_pool* pool, int32_t n_tokens, const int32_t* d_req,
  *  d_topk [n, K] int32 out: the K highest scores, ties to the lower token, in
  *  ascending token order; -1 pads when limit < K.
  *  d_scores nullable [n, max_ctx] int64 out, 16-byte aligned: every score (entries >= limit
- *  undefined). */
+ *  undefined).
+ * Selection on the whole GPU: with few query tokens the top-K selection spreads each
+ * token over up to one CTA per SM and synchronises them with bounded grid-wide
+ * waits, which needs every one of those CTAs resident at once. Work on other streams
+ * that holds SMs for longer than the one-second wait limit makes the call fail with
+ * HS_ERR_TIMEOUT (read by hs_get_error, which also clears the selection scratch the
+ * timed-out call left). hs_set_select_mode(pool, HS_SELECT_LOCAL) avoids this path
+ * for engines that share the GPU; the no-allocation variant below never uses it. */
+hs_status hs_indexer_topk(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
+                          const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
+                          const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,
+                          hs_stream_t stream);
+
 /* FP8 indexer and top-K for a pool with idx_format HS_IDX_FP8 ([P2] footnote 3:
  * keys of 128 FP8 values and a 4-byte scale). Per query token j and earlier
  * token t:
@@ -225,11 +238,6 @@ hs_status hs_append_rows(hs_pool* pool, int32_t n_tokens, const int32_t* d_req,
 hs_status hs_indexer_topk_fp8(hs_pool* pool, int32_t index_layer, int32_t n_tokens, const int32_t* d_req,
                               const int32_t* d_limit, const uint8_t* d_q, const float* d_w, int32_t* d_topk,
                               float* d_scores, hs_stream_t stream);
-
-hs_status hs_indexer_topk(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
-                          const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
-                          const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,
-                          hs_stream_t stream);
 
 /* Fused top-K resolver for indexer group `group` at step `step` ([P1] "How it
  * works"): for the union of the selected tokens of each request, a resident page
@@ -319,9 +327,38 @@ hs_status hs_indexer_topk_noalloc(hs_pool* pool, int32_t index_layer, int32_t n_
  * status word and returns, leaving the context usable. Asynchronous. */
 hs_status hs_wait_selftest(hs_pool* pool, hs_stream_t stream);
 
+/* Self-test of the selection's failure path (not part of the decode step). Runs the
+ * grid-wide top-K selection again over the scores the pool's last hs_indexer_topk
+ * (or hs_indexer_topk_fp8) call left in its scratch (a call made with d_scores
+ * NULL), with one CTA of each query token never arriving at the grid-wide waits, as
+ * when work on another stream holds an SM. The token's other CTAs give up after
+ * about one second: HS_ERR_TIMEOUT in the device status word and a half-used
+ * selection scratch, which later selections route around (correct, slower) until
+ * hs_get_error reports the timeout and clears it. d_limit [n] as for the indexer;
+ * d_topk [n, K] receives undefined values. HS_ERR_INVALID when n tokens would not
+ * take the grid-wide selection. Asynchronous. */
+hs_status hs_select_selftest(hs_pool* pool, int32_t n_tokens, const int32_t* d_limit, int32_t* d_topk,
+                             hs_stream_t stream);
+
 /* Synchronise stream, return the first device-detected error since the last
- * call in *device_status and clear it. */
+ * call in *device_status and clear it. When it is HS_ERR_TIMEOUT, the selection
+ * scratch a timed-out grid-wide wait may have left half used is also cleared, so
+ * later calls run at full speed again (until then they select correctly on a
+ * slower path that uses no scratch). The pool's calls must be issued on one
+ * stream at a time. */
 hs_status hs_get_error(hs_pool* pool, hs_status* device_status, hs_stream_t stream);
+
+/* Selection modes (hs_set_select_mode).
+ * HS_SELECT_AUTO   (default) few query tokens are selected by groups of CTAs spread
+ *                  over every SM with bounded grid-wide waits (fastest when the
+ *                  pool's calls have the GPU to themselves);
+ * HS_SELECT_LOCAL  no selection waits on CTAs of other SMs: one CTA, or one
+ *                  cluster of CTAs, per query token. For engines that run other
+ *                  work on the GPU at the same time. */
+#define HS_SELECT_AUTO 0
+#define HS_SELECT_LOCAL 1
+/* Host-side, between steps. HS_ERR_INVALID for an unknown mode. */
+hs_status hs_set_select_mode(hs_pool* pool, int32_t mode);
 
 /* Synchronise stream and read the device counters (reset = nonzero clears them). */
 hs_status hs_get_counters(hs_pool* pool, hs_counters* out, int32_t reset, hs_stream_t stream);

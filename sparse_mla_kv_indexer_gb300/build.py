@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhisparse.so")
 SOURCES = ["hs_pool.cu", "hs_indexer.cu", "hs_indexer_fp8.cu", "hs_select_wide.cu", "hs_resolver.cu", "hs_attention.cu",
-           "hs_noalloc.cu"]
+           "hs_attention_seq.cu", "hs_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

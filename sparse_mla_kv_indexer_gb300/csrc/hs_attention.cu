@@ -609,6 +609,8 @@ static hs_status launch_attention_hpc(hs_pool* p, int layer, int n, int n_splits
 
 hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows, float sm_scale,
                            uint16_t* d_out, float* d_lse, bool settled, cudaStream_t st) {
+  // many query tokens: one CTA per token over all its rows (hs_attention_seq.cu)
+  if (attention_seq_suits(p, n)) return launch_attention_seq(p, layer, n, d_q, d_rows, sm_scale, d_out, d_lse, st);
   const int n_splits = (p->cfg.topk + ATTN_ROWS - 1) / ATTN_ROWS;
   const int H = p->cfg.n_heads;
   // fewer heads per CTA while the head groups still fit on the SMs side by side

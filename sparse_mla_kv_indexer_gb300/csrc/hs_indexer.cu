@@ -219,7 +219,13 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
   const uint32_t tmem = *tmem_slot;
   const int nseg = *s_nseg;
   const int total = nseg ? segs[nseg - 1].tile_end : 0;
-  const int n_local = total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // Each CTA takes a contiguous run of tiles: in a batch of requests a CTA then meets
+  // one or two request boundaries in the whole launch, and each boundary drains its
+  // pipeline (the query operand and the head weights of the next request are loaded
+  // once the previous request's MMAs and epilogues are done).
+  const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int first_item = (int)blockIdx.x * per;
+  const int n_local = total > first_item ? min(per, total - first_item) : 0;
 
   auto seg_of = [&](int item) {
     int lo = 0, hi = nseg - 1;
@@ -229,7 +235,7 @@ indexer_kernel(Dev D, int il, int n_tok, const int32_t* __restrict__ req_of, con
     }
     return lo;
   };
-  auto item_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
+  auto item_of = [&](int i) { return first_item + i; };
 
   if (warp == IX_PRODUCER_WARP) {
     // ------------------------------ producer ------------------------------
@@ -863,7 +869,7 @@ hs_status launch_select_cl(hs_pool* p, int n, const int64_t* scores, int ld, con
 int select_wide_groups(hs_pool* p, int n, bool wide_ok) {
   // few query tokens: one wide group of co-resident CTAs per token, all SMs busy
   const int sms = num_sms(), g_min = sel_wide_min_g(p->cfg.max_ctx);
-  if (!wide_ok || n < 1 || n > p->d.sel_ws_tokens || n * g_min > sms) return 0;
+  if (!wide_ok || p->select_mode != HS_SELECT_AUTO || n < 1 || n > p->d.sel_ws_tokens || n * g_min > sms) return 0;
   int G = sms / n;
   if (G > SW_MAX_G) G = SW_MAX_G;
   const int g_want = (p->cfg.max_ctx + SW_TARGET - 1) / SW_TARGET;
@@ -880,6 +886,8 @@ hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const 
                         int32_t* d_topk, cudaStream_t st, bool fp_keys, bool wide_ok, bool hist0_done) {
   const int G = select_wide_groups(p, n, wide_ok);
   if (G > 0) return launch_select_wide(p, n, scores, ld, d_limit, d_topk, fp_keys, G, hist0_done, st);
+  // many query tokens: one CTA per token, every token at once
+  if (wide_ok && n > num_sms() / 8) return launch_select_token(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
   // otherwise 16 CTAs per token: each CTA's chunk is smaller and every pass shorter
   return launch_select_cl<16>(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
 }

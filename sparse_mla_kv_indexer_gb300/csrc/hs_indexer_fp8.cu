@@ -97,7 +97,8 @@ __device__ __forceinline__ void f8_arrive(uint32_t bar) {
 }
 
 __global__ void __launch_bounds__(F8_THREADS, 1)
-indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int n_tok,
+indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap2,
+                   const __grid_constant__ CUtensorMap smap2, int il, int n_tok,
                    const int32_t* __restrict__ req_of, const int32_t* __restrict__ limit_of,
                    const uint8_t* __restrict__ qg, const float* __restrict__ wg, long long* __restrict__ keys_out,
                    float* __restrict__ scores_out, int ld, F8Layout L, uint32_t* __restrict__ hist0) {
@@ -180,7 +181,13 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
   const uint32_t tmem = *tmem_slot;
   const int nseg = *s_nseg;
   const int total = nseg ? segs[nseg - 1].tile_end : 0;
-  const int n_local = total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // Each CTA takes a contiguous run of tiles: in a batch of requests a CTA then meets
+  // one or two request boundaries in the whole launch, and each boundary drains its
+  // pipeline (the query operand and the head weights of the next request are loaded
+  // once the previous request's MMAs and epilogues are done).
+  const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int first_item = (int)blockIdx.x * per;
+  const int n_local = total > first_item ? min(per, total - first_item) : 0;
   auto seg_of = [&](int item) {
     int lo = 0, hi = nseg - 1;
     while (lo < hi) {
@@ -189,7 +196,7 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
     }
     return lo;
   };
-  auto item_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
+  auto item_of = [&](int i) { return first_item + i; };
 
   if (warp == F8_PRODUCER_WARP) {
     // ------------------------------ producer ------------------------------
@@ -238,12 +245,22 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, int il, int 
           }
           mbar_expect_tx(bar, bytes);
           mbar_expect_tx(cbar, bytes / IDX_DIM * 4);
-          for (int k = 0; k < 2; ++k)
-            if (ips[k] >= 0 && ips[k] < D.num_idx_pages) {
-              tma_load_2d(smem_u32(stage + k * PAGE * IDX_DIM), &tmap, 0, ips[k] * F8_PAGE_ROWS, bar);
-              bulk_g2s(smem_u32(slot + k * PAGE * 4),
-                       keys + (size_t)ips[k] * HS_IDX_FP8_PAGE_BYTES + PAGE * IDX_DIM, PAGE * 4, cbar);
-            }
+          // Copies take about the same time whatever their size up to 16-32 KB (the
+          // SM's copy engine serialises them), so two adjacent pages -- the usual case,
+          // a request's always-resident key cache is allocated in runs -- come with one
+          // 3-D tensor load for their key rows and one 2-D load for their scales.
+          const bool ok0 = ips[0] >= 0 && ips[0] < D.num_idx_pages, ok1 = ips[1] >= 0 && ips[1] < D.num_idx_pages;
+          if (ok0 && ok1 && ips[1] == ips[0] + 1) {
+            tma_load_3d(smem_u32(stage), &tmap2, 0, 0, ips[0], bar);
+            tma_load_2d(smem_u32(slot), &smap2, 0, ips[0], cbar);
+          } else {
+            for (int k = 0; k < 2; ++k)
+              if (k == 0 ? ok0 : ok1) {
+                tma_load_2d(smem_u32(stage + k * PAGE * IDX_DIM), &tmap, 0, ips[k] * F8_PAGE_ROWS, bar);
+                bulk_g2s(smem_u32(slot + k * PAGE * 4),
+                         keys + (size_t)ips[k] * HS_IDX_FP8_PAGE_BYTES + PAGE * IDX_DIM, PAGE * 4, cbar);
+              }
+          }
           *s_issued = i + 1;
         }
       }
@@ -405,10 +422,10 @@ hs_status launch_indexer_fp8(hs_pool* p, int il, int n, const int32_t* d_req, co
   const F8Layout L = f8_layout(n_max, p->cfg.max_tokens, d_hist0 != nullptr);
   // alternate tiles go to alternate epilogue warpgroups: an even accumulator count
   // keeps every accumulator with one warpgroup, so its phase waits never alias
-  if (L.stages < 2 || L.n_acc % F8_EPI_GROUPS || il < 0 || il >= (int)p->idx_tmaps.size()) return HS_ERR_INVALID;
+  if (L.stages < 2 || L.n_acc % F8_EPI_GROUPS || il < 0 || 3 * il + 2 >= (int)p->idx_tmaps.size()) return HS_ERR_INVALID;
   if (ensure_kernel_attrs(indexer_fp8_kernel, L.smem) != HS_OK) return HS_ERR_CUDA;
-  return launch_pdl(indexer_fp8_kernel, dim3(num_sms()), dim3(F8_THREADS), L.smem, st, 0, p->d, p->idx_tmaps[il],
-                    il, n, d_req, d_limit, d_q, d_w, reinterpret_cast<long long*>(d_keys), d_scores,
+  return launch_pdl(indexer_fp8_kernel, dim3(num_sms()), dim3(F8_THREADS), L.smem, st, 0, p->d,
+                    p->idx_tmaps[3 * il], p->idx_tmaps[3 * il + 1], p->idx_tmaps[3 * il + 2], il, n, d_req, d_limit, d_q, d_w, reinterpret_cast<long long*>(d_keys), d_scores,
                     p->cfg.max_ctx, L, d_hist0);
 }
 

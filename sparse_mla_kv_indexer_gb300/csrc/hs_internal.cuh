@@ -69,12 +69,16 @@ struct hs_pool {
   int device;
   std::vector<int32_t> n_hot_host;   // leased pages per (req, group), mirrored on the host
   std::vector<void*> allocations;
-  std::vector<CUtensorMap> idx_tmaps;   // HS_IDX_FP8: one per indexer layer, 128-byte swizzled key pages
+  // HS_IDX_FP8, three per indexer layer: one page's 64 key rows (2-D, 128-byte
+  // swizzled), two adjacent pages' key rows (3-D: the scale rows between them are
+  // skipped), two adjacent pages' scales (2-D, 256 bytes per page)
+  std::vector<CUtensorMap> idx_tmaps;
   // The last hot-path launch of this pool was hs_sparse_mla_decode over settled_rows
   // on settled_stream (null: it was something else). A decode that follows it with
   // the same rows on the same stream may read them before that kernel completes.
   const void* settled_rows = nullptr;
   void* settled_stream = nullptr;
+  int32_t select_mode = HS_SELECT_AUTO;   // hs_set_select_mode
 };
 
 namespace hs {
@@ -174,6 +178,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
           "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// 3-D tiled tensor load (TMA) of the box at (x, y, z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
@@ -452,6 +464,10 @@ hs_status launch_replay(hs_pool* p, int group, int n, const int32_t* d_req, cons
 // the stream, which is a decode of the same rows (see hs_pool::settled_rows)
 hs_status launch_attention(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows,
                            float sm_scale, uint16_t* d_out, float* d_lse, bool settled, cudaStream_t st);
+// the one-CTA-per-token attention for many query tokens (64 heads)
+bool attention_seq_suits(const hs_pool* p, int n);
+hs_status launch_attention_seq(hs_pool* p, int layer, int n, const uint16_t* d_q, const int32_t* d_rows,
+                               float sm_scale, uint16_t* d_out, float* d_lse, cudaStream_t st);
 int num_sms();
 
 }  // namespace hs

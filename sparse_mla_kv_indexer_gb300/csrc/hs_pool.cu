@@ -219,6 +219,7 @@ const char* hs_status_string(hs_status s) {
     case HS_ERR_BAD_WEIGHT: return "negative index-head weight";
     case HS_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation indexer";
     case HS_ERR_NOT_RESOLVED: return "replayed token is neither resident nor in the hot buffer";
+    case HS_ERR_RANGE: return "attention input beyond the fp16 range of the batched path";
   }
   return "unknown status";
 }
@@ -240,14 +241,32 @@ static hs_status make_key_tensor_maps(hs_pool* p, void* const* d_idx_layers) {
       return HS_ERR_CUDA;
     encode = reinterpret_cast<EncodeFn>(fn);
   }
-  p->idx_tmaps.resize(p->d.n_groups);
+  p->idx_tmaps.resize(3 * (size_t)p->d.n_groups);
+  const cuuint64_t np = (cuuint64_t)p->cfg.num_idx_pages;
+  const cuuint32_t estr[3] = {1, 1, 1};
   for (int g = 0; g < p->d.n_groups; ++g) {
-    const cuuint64_t dims[2] = {128, (cuuint64_t)p->cfg.num_idx_pages * (HS_IDX_FP8_PAGE_BYTES / 128)};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, (cuuint32_t)PAGE};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&p->idx_tmaps[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d_idx_layers[g], dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUtensorMap* m = &p->idx_tmaps[3 * (size_t)g];
+    uint8_t* base = static_cast<uint8_t*>(d_idx_layers[g]);
+    // one page: rows of 128 bytes over the whole cache, box of the page's 64 key rows
+    const cuuint64_t dims1[2] = {128, np * (HS_IDX_FP8_PAGE_BYTES / 128)};
+    const cuuint64_t str1[1] = {128};
+    const cuuint32_t box1[2] = {128, (cuuint32_t)PAGE};
+    // two adjacent pages: (128 bytes, 64 key rows, page), page stride 8,448 bytes
+    const cuuint64_t dims2[3] = {128, (cuuint64_t)PAGE, np};
+    const cuuint64_t str2[2] = {128, HS_IDX_FP8_PAGE_BYTES};
+    const cuuint32_t box2[3] = {128, (cuuint32_t)PAGE, 2};
+    // the 256 scale bytes of two adjacent pages
+    const cuuint64_t dims3[2] = {(cuuint64_t)PAGE * 4, np};
+    const cuuint64_t str3[1] = {HS_IDX_FP8_PAGE_BYTES};
+    const cuuint32_t box3[2] = {(cuuint32_t)PAGE * 4, 2};
+    if (encode(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims1, str1, box1, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims2, str2, box2, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&m[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base + PAGE * IDX_DIM, dims3, str3, box3, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return HS_ERR_INVALID;
   }
@@ -541,6 +560,16 @@ hs_status hs_wait_selftest(hs_pool* p, hs_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
+hs_status hs_select_selftest(hs_pool* p, int32_t n, const int32_t* d_limit, int32_t* d_topk, hs_stream_t stream) {
+  CallRange nvtx_range("hs_select_selftest");
+  if (!p || !d_limit || !d_topk || n < 1 || n > p->cfg.max_tokens) return HS_ERR_INVALID;
+  const int G = select_wide_groups(p, n, true);
+  if (G == 0) return HS_ERR_INVALID;
+  p->settled_rows = nullptr;
+  return launch_select_wide(p, n, p->d.scores, p->cfg.max_ctx, d_limit, d_topk, p->d.idx_fmt == HS_IDX_FP8, G, false,
+                            reinterpret_cast<cudaStream_t>(stream), true);
+}
+
 hs_status hs_get_error(hs_pool* p, hs_status* device_status, hs_stream_t stream) {
   CallRange nvtx_range("hs_get_error");
   if (!p || !device_status) return HS_ERR_INVALID;
@@ -549,7 +578,21 @@ hs_status hs_get_error(hs_pool* p, hs_status* device_status, hs_stream_t stream)
   int32_t v = 0;
   HS_CUDA_TRY(cudaMemcpy(&v, p->d.status, sizeof(v), cudaMemcpyDeviceToHost));
   HS_CUDA_TRY(cudaMemset(p->d.status, 0, sizeof(int32_t)));
+  if (v == HS_ERR_TIMEOUT && p->d.sel_ws) {
+    // a grid-wide wait of the selection may have given up half way: start its scratch
+    // (arrival counters, histogram sums, candidate list, the flag that routes later
+    // selections around it) from zero again
+    HS_CUDA_TRY(cudaMemset(p->d.sel_ws, 0, (size_t)p->d.sel_ws_tokens * sizeof(SelWs)));
+    HS_CUDA_TRY(cudaDeviceSynchronize());
+  }
   *device_status = static_cast<hs_status>(v);
+  return HS_OK;
+}
+
+hs_status hs_set_select_mode(hs_pool* p, int32_t mode) {
+  CallRange nvtx_range("hs_set_select_mode");
+  if (!p || (mode != HS_SELECT_AUTO && mode != HS_SELECT_LOCAL)) return HS_ERR_INVALID;
+  p->select_mode = mode;
   return HS_OK;
 }
 

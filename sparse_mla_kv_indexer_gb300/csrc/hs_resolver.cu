@@ -85,6 +85,9 @@ __device__ void bitonic_sort(T* a, int n) {
 constexpr int RS_COPY_CTAS = 8;      // CTAs of a request's cluster that copy its missed rows
 constexpr int RS_COPY_UNROLL = 4;    // 16-byte host loads in flight per thread
 
+// CL: CTAs per request segment (a thread-block cluster when CL > 1) that copy its
+// missed rows; the first resolves.
+template <int CL>
 __global__ void __launch_bounds__(RS_THREADS, 1)
 resolve_kernel(Dev D, int group, int step, int n_tok, const int32_t* __restrict__ req_of,
                const int32_t* __restrict__ topk, int32_t* __restrict__ row_ids, hs_plan_entry* __restrict__ plan) {
@@ -470,13 +473,14 @@ resolve_kernel(Dev D, int group, int step, int n_tok, const int32_t* __restrict_
 
   // ---- 6. every CTA of the cluster copies its share of the missed rows of every
   //         layer of the group from the mapped host pool (records in rank 0) ----
-  cluster_sync();   // rank 0's records are complete
-  const int n_rec = (int)ld_cluster_u32(mapa(smem_u32(&s_listed), 0));
+  if constexpr (CL > 1) cluster_sync();   // rank 0's records are complete
+  else __syncthreads();
+  const int n_rec = CL > 1 ? (int)ld_cluster_u32(mapa(smem_u32(&s_listed), 0)) : s_listed;
   if (n_rec > 0) {
-    const uint32_t recs = mapa(smem_u32(V), 0);
+    const uint32_t recs = CL > 1 ? mapa(smem_u32(V), 0) : 0u;
     const int64_t* hpr = D.host_pg + (size_t)r * D.max_pages;
     const long long total = (long long)n_rec * n_lg * ROW_CHUNKS;
-    const long long stride = (long long)RS_COPY_CTAS * RS_THREADS;
+    const long long stride = (long long)CL * RS_THREADS;
     for (long long c0 = (long long)rank * RS_THREADS + tid; c0 < total; c0 += stride * RS_COPY_UNROLL) {
       uint4 v[RS_COPY_UNROLL];
       uint8_t* dst[RS_COPY_UNROLL];
@@ -489,7 +493,7 @@ resolve_kernel(Dev D, int group, int step, int n_tok, const int32_t* __restrict_
         const int part = (int)(c - row_i * ROW_CHUNKS);
         const int m = (int)(row_i / n_lg);
         const int layer = lo_layer + (int)(row_i - (long long)m * n_lg);
-        const unsigned long long rec = ld_cluster_u64(recs + 8u * (uint32_t)m);
+        const unsigned long long rec = CL > 1 ? ld_cluster_u64(recs + 8u * (uint32_t)m) : V[m];
         if (rec == ~0ull) continue;
         const int t = (int)(uint32_t)rec, prow = (int)(rec >> 32);
         const int64_t hp = hpr[t >> 6];
@@ -502,17 +506,25 @@ resolve_kernel(Dev D, int group, int step, int n_tok, const int32_t* __restrict_
         if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = v[u];
     }
   }
-  cluster_sync();   // rank 0's shared memory is read by its peers until here
+  if constexpr (CL > 1) cluster_sync();   // rank 0's shared memory is read by its peers until here
 }
 
 constexpr int RS_SMEM = RS_MAXU * (4 + 4 + 4 + 1 + 8);
 
 hs_status launch_resolve(hs_pool* p, int group, int step, int n, const int32_t* d_req, const int32_t* d_topk,
                          int32_t* d_row_ids, hs_plan_entry* d_plan, cudaStream_t st) {
-  if (ensure_kernel_attrs(resolve_kernel, RS_SMEM) != HS_OK) return HS_ERR_CUDA;
-  // one cluster of RS_COPY_CTAS CTAs per token (the first token of each request resolves it)
-  return launch_pdl_cluster(resolve_kernel, dim3(n, RS_COPY_CTAS), dim3(RS_THREADS), RS_SMEM, st,
-                            dim3(1, RS_COPY_CTAS, 1), p->d, group, step, n, d_req, d_topk, d_row_ids, d_plan);
+  // Few query tokens: one cluster of RS_COPY_CTAS CTAs per token (the first token of
+  // each request resolves it, the cluster copies its misses). Many tokens: one CTA per
+  // token, so that every request resolves in the same wave of CTAs (a CTA takes a
+  // whole SM's shared memory).
+  if ((long long)n * RS_COPY_CTAS <= num_sms()) {
+    if (ensure_kernel_attrs(resolve_kernel<RS_COPY_CTAS>, RS_SMEM) != HS_OK) return HS_ERR_CUDA;
+    return launch_pdl_cluster(resolve_kernel<RS_COPY_CTAS>, dim3(n, RS_COPY_CTAS), dim3(RS_THREADS), RS_SMEM, st,
+                              dim3(1, RS_COPY_CTAS, 1), p->d, group, step, n, d_req, d_topk, d_row_ids, d_plan);
+  }
+  if (ensure_kernel_attrs(resolve_kernel<1>, RS_SMEM) != HS_OK) return HS_ERR_CUDA;
+  return launch_pdl(resolve_kernel<1>, dim3(n, 1), dim3(RS_THREADS), RS_SMEM, st, 0, p->d, group, step, n, d_req,
+                    d_topk, d_row_ids, d_plan);
 }
 
 // Replay: each (token, k) looked up in the residency maps as they stand; read only.

@@ -101,7 +101,8 @@ struct SelWs {
   unsigned long long bar;             // grid-barrier arrivals, all launches
   unsigned long long base;            // bar at the start of the next launch
   uint32_t ncand;                     // keys of the final range appended to cand
-  uint32_t pad[3];
+  uint32_t dirty;                     // a launch gave up at a grid-wide wait; cleared by hs_get_error
+  uint32_t pad[2];
   uint32_t above[SW_MAX_G];           // per CTA: its keys above the final range
   uint32_t hist[SW_LEVELS][SEL_BINS]; // per level: sum of the CTAs' histograms
   unsigned long long cand[SW_CAND];
@@ -114,7 +115,12 @@ inline int sel_wide_min_g(int max_ctx) {
 }
 
 // hist0_done: the level-0 histogram sums of the (single) token are already complete
+// withhold: the failure-path self-test (one CTA per token never arrives at the waits)
 hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                             int32_t* d_topk, bool fp_keys, int G, bool hist0_done, cudaStream_t st);
+                             int32_t* d_topk, bool fp_keys, int G, bool hist0_done, cudaStream_t st,
+                             bool withhold = false);
+// one CTA per query token, no cross-CTA waits (many tokens)
+hs_status launch_select_token(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                              int32_t* d_topk, bool fp_keys, cudaStream_t st);
 
 }  // namespace hs

@@ -33,7 +33,8 @@ namespace {
 // Grid barrier of the G CTAs of one query token: wait until the arrival counter
 // reaches `target`. After WAIT_NS the status records HS_ERR_TIMEOUT and false is
 // returned to every thread of the CTA.
-__device__ bool sw_barrier(unsigned long long* ctr, unsigned long long target, int32_t* status, int* s_ok) {
+__device__ bool sw_barrier(SelWs* W, unsigned long long target, int32_t* status, int* s_ok) {
+  unsigned long long* ctr = &W->bar;
   __syncthreads();
   if (threadIdx.x == 0) {
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
@@ -49,6 +50,7 @@ __device__ bool sw_barrier(unsigned long long* ctr, unsigned long long target, i
           t0 = now;
         } else if (now - t0 > WAIT_NS) {
           set_status(status, HS_ERR_TIMEOUT);
+          atomicExch(&W->dirty, 1u);   // this token's scratch is left half used
           ok = 0;
           break;
         }
@@ -99,9 +101,201 @@ __device__ __forceinline__ bool in_range(unsigned long long k, unsigned long lon
   return k >= base && k - base < width;
 }
 
+// ---- one CTA selects the top K of one token, streaming its keys from global memory ----
+// Warp w owns a contiguous range of the token's keys (a multiple of 512 keys, so
+// every lane reads 16 keys with eight 16-byte loads, all in flight at once), so the
+// emit pass can write its selected tokens in ascending order at a known offset.
+// Passes over the keys (reads from L2): the level-0 histogram, further histogram
+// levels while the range holding the K-th largest key has more than SW_CAND keys,
+// the collection of that range (each warp also counts its keys above it), and the
+// emit pass.
+constexpr int ST_PER_LANE = 16;
+constexpr int ST_SPAN = 32 * ST_PER_LANE;   // keys per warp step
+
+// The ST_PER_LANE keys of a lane at i (a multiple of 16); keys at or beyond `hi` are 0 and
+// flagged invalid (bit k of the returned mask set for a valid key k).
+__device__ __forceinline__ uint32_t st_load_lane(const long long* s, int i, int hi,
+                                                unsigned long long (&k)[ST_PER_LANE], int32_t* status) {
+  longlong2 v[ST_PER_LANE / 2];
+#pragma unroll
+  for (int j = 0; j < ST_PER_LANE / 2; ++j)
+    v[j] = i + 2 * j < hi ? __ldcg(reinterpret_cast<const longlong2*>(s + i) + j) : make_longlong2(0, 0);
+  uint32_t valid = 0;
+#pragma unroll
+  for (int j = 0; j < ST_PER_LANE; ++j) {
+    long long x = (j & 1) ? v[j >> 1].y : v[j >> 1].x;
+    if (i + j < hi) {
+      valid |= 1u << j;
+      if (x < 0) {
+        set_status(status, HS_ERR_BAD_WEIGHT);
+        x = 0;
+      }
+    }
+    k[j] = sel_key(x, i + j);
+  }
+  return valid;
+}
+
+__device__ void select_token_cta(const long long* __restrict__ s, int n, int K, bool fp_keys, int32_t* __restrict__ out,
+                                 int32_t* status, uint32_t* hist, unsigned long long* cand, int* warp_tot,
+                                 int* s_small) {
+  constexpr int NW = SW_THREADS / 32;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int* s_bin = s_small;
+  int* s_cnt = s_small + 1;
+  int* w_above = s_small + 2;            // [NW] keys above the final range in warp w's range
+  int* w_off = w_above + NW;             // [NW] output offset of warp w
+  long long* s_above = reinterpret_cast<long long*>(s_small + 2 + 2 * NW + 2);
+  unsigned long long* s_tau = reinterpret_cast<unsigned long long*>(s_above + 1);
+  if (n <= K) {
+    for (int i = tid; i < K; i += SW_THREADS) out[i] = i < n ? i : -1;
+    return;
+  }
+  const int wper = (n + NW * ST_SPAN - 1) / (NW * ST_SPAN) * ST_SPAN;
+  const int wlo = min(n, wid * wper), whi = min(n, wlo + wper);
+  unsigned long long k[ST_PER_LANE];
+  // level 0
+  for (int b = tid; b < SEL_BINS; b += SW_THREADS) hist[b] = 0;
+  __syncthreads();
+  for (int i0 = wlo; i0 < whi; i0 += ST_SPAN) {
+    const uint32_t v = st_load_lane(s, i0 + lane * ST_PER_LANE, whi, k, status);
+#pragma unroll
+    for (int j = 0; j < ST_PER_LANE; ++j)
+      if (v >> j & 1) atomicAdd(&hist[bucket_of(k[j], fp_keys)], 1u);
+  }
+  __syncthreads();
+  int need = K;
+  sw_find<false>(hist, need, warp_tot, s_bin, s_above);
+  unsigned long long base, width;
+  bucket_range(*s_bin, fp_keys, base, width);
+  int n_range = (int)hist[*s_bin];
+  need -= (int)*s_above;
+  while (n_range > SW_CAND && width > 1) {
+    const int shift = refine_shift(width);
+    __syncthreads();
+    for (int b = tid; b < SEL_BINS; b += SW_THREADS) hist[b] = 0;
+    __syncthreads();
+    for (int i0 = wlo; i0 < whi; i0 += ST_SPAN) {
+      const uint32_t v = st_load_lane(s, i0 + lane * ST_PER_LANE, whi, k, status);
+#pragma unroll
+      for (int j = 0; j < ST_PER_LANE; ++j)
+        if ((v >> j & 1) && in_range(k[j], base, width)) atomicAdd(&hist[(int)((k[j] - base) >> shift)], 1u);
+    }
+    __syncthreads();
+    sw_find<false>(hist, need, warp_tot, s_bin, s_above);
+    n_range = (int)hist[*s_bin];
+    base += (unsigned long long)*s_bin << shift;
+    need -= (int)*s_above;
+    width = 1ull << shift;
+  }
+  // the final range to shared memory; each warp counts its keys above the range
+  if (tid == 0) *s_cnt = 0;
+  __syncthreads();
+  int above = 0;
+  for (int i0 = wlo; i0 < whi; i0 += ST_SPAN) {
+    const uint32_t v = st_load_lane(s, i0 + lane * ST_PER_LANE, whi, k, status);
+#pragma unroll
+    for (int j = 0; j < ST_PER_LANE; ++j) {
+      if (!(v >> j & 1) || k[j] < base) continue;
+      if (k[j] - base < width) {
+        const int at = atomicAdd(s_cnt, 1);
+        if (at < SW_CAND) cand[at] = k[j];
+      } else {
+        ++above;
+      }
+    }
+  }
+  above = __reduce_add_sync(0xffffffffu, above);
+  if (lane == 0) w_above[wid] = above;
+  __syncthreads();
+  // tau: the need-th largest key of the range
+  const int nc = min(*s_cnt, SW_CAND);
+  int lcnt = nc, lneed = need;
+  while (lcnt > 1 && width > 1) {
+    const int shift = refine_shift(width);
+    for (int b = tid; b < SEL_BINS; b += SW_THREADS) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < nc; i += SW_THREADS)
+      if (in_range(cand[i], base, width)) atomicAdd(&hist[(int)((cand[i] - base) >> shift)], 1u);
+    __syncthreads();
+    sw_find<false>(hist, lneed, warp_tot, s_bin, s_above);
+    lcnt = (int)hist[*s_bin];
+    base += (unsigned long long)*s_bin << shift;
+    lneed -= (int)*s_above;
+    width = 1ull << shift;
+    __syncthreads();
+  }
+  if (tid == 0) *s_tau = base;
+  __syncthreads();
+  if (width > 1)   // a single key is left in [base, base + width): it is tau
+    for (int i = tid; i < nc; i += SW_THREADS)
+      if (in_range(cand[i], base, width)) *s_tau = cand[i];
+  __syncthreads();
+  const unsigned long long tau = *s_tau;
+  // output offsets: per warp range, its keys above the range plus its range keys >= tau
+  if (tid < NW) w_off[tid] = w_above[tid];
+  __syncthreads();
+  for (int i = tid; i < nc; i += SW_THREADS)
+    if (cand[i] >= tau) atomicAdd(&w_off[min(NW - 1, sel_token(cand[i]) / wper)], 1);
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int w = 0; w < NW; ++w) {
+      const int c = w_off[w];
+      w_off[w] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  // emit: the lanes of a warp hold 16 consecutive keys each, so a lane's selected keys
+  // follow those of the lanes before it
+  int wbase = w_off[wid];
+  for (int i0 = wlo; i0 < whi; i0 += ST_SPAN) {
+    const int i = i0 + lane * ST_PER_LANE;
+    const uint32_t v = st_load_lane(s, i, whi, k, status);
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < ST_PER_LANE; ++j) c += (v >> j & 1) && k[j] >= tau;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int pos = wbase + incl - c;
+#pragma unroll
+    for (int j = 0; j < ST_PER_LANE; ++j)
+      if ((v >> j & 1) && k[j] >= tau) {
+        if (pos < K) out[pos] = i + j;
+        else set_status(status, HS_ERR_BAD_ID);
+        ++pos;
+      }
+    wbase += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
+// Many query tokens: one CTA per token (grid-stride over tokens), no cross-CTA waits.
+__global__ void __launch_bounds__(SW_THREADS, 1)
+select_token_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of,
+                    int32_t* __restrict__ topk, int n_tok, int fp_keys) {
+  __shared__ __align__(16) uint32_t hist[SEL_BINS];
+  __shared__ __align__(16) unsigned long long cand[SW_CAND];
+  __shared__ int warp_tot[32];
+  __shared__ __align__(16) int s_small[2 + 2 * (SW_THREADS / 32) + 2 + 4];
+  griddep_wait();
+  griddep_launch();
+  for (int tok = blockIdx.x; tok < n_tok; tok += gridDim.x) {
+    int n = limit_of[tok];
+    n = max(0, min(n, D.max_ctx));
+    select_token_cta(reinterpret_cast<const long long*>(scores) + (size_t)tok * ld, n, D.topk, fp_keys != 0,
+                     topk + (size_t)tok * D.topk, D.status, hist, cand, warp_tot, s_small);
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(SW_THREADS, 1)
 select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of,
-                   int32_t* __restrict__ topk, int fp_keys, int G, int hist0_done) {
+                   int32_t* __restrict__ topk, int fp_keys, int G, int hist0_done, int withhold) {
   const int tok = blockIdx.x / G, g = blockIdx.x - tok * G;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int K = D.topk;
@@ -112,6 +306,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   __shared__ long long s_above;
   __shared__ unsigned long long s_tau;
   __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(16) int dirty_small[2 + 2 * (SW_THREADS / 32) + 2 + 4];
   extern __shared__ __align__(16) uint8_t sw_dyn[];
   unsigned long long* cache = reinterpret_cast<unsigned long long*>(sw_dyn);   // [SW_CHUNK] keys
   unsigned long long* cand = cache + SW_CHUNK;                                  // [SW_CAND] final range
@@ -128,6 +323,16 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   int n = limit_of[tok];
   n = max(0, min(n, D.max_ctx));
   int32_t* out = topk + (size_t)tok * K;
+  if (__ldcg(&W->dirty)) {
+    // An earlier launch gave up at a grid-wide wait and left this token's scratch
+    // half used. Until hs_get_error has reported that and cleared the scratch, the
+    // token is selected by its first CTA alone, without the scratch and without waits.
+    griddep_launch();
+    if (g == 0)
+      select_token_cta(reinterpret_cast<const long long*>(scores) + (size_t)tok * ld, n, K, fp_keys != 0, out,
+                       D.status, hist, cand, warp_tot, dirty_small);
+    return;
+  }
   // a launch that returns before the barriers clears the sums the scoring kernel filled
   auto clear_hist0 = [&]() {
     if (hist0_done)
@@ -146,6 +351,12 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     griddep_launch();
     clear_hist0();
     if (g == 0 && tid == 0) set_status(D.status, HS_ERR_BAD_ID);
+    return;
+  }
+  if (withhold && g == G - 1) {
+    // self-test of the failure path: this CTA never arrives at the grid-wide waits,
+    // as if it could not get an SM, so the token's other CTAs give up after WAIT_NS
+    griddep_launch();
     return;
   }
   const long long* s = reinterpret_cast<const long long*>(scores) + (size_t)tok * ld;
@@ -180,7 +391,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     __syncthreads();
     for (int b = tid; b < SEL_BINS; b += SW_THREADS)
       if (hist[b]) atomicAdd(&W->hist[0][b], hist[b]);
-    if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
+    if (!sw_barrier(W, bar0 + ++nbar * G, D.status, &s_ok)) return;
     griddep_launch();
     resident = true;
   }
@@ -207,7 +418,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     __syncthreads();
     for (int b = tid; b < SEL_BINS; b += SW_THREADS)
       if (hist[b]) atomicAdd(&W->hist[level][b], hist[b]);
-    if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
+    if (!sw_barrier(W, bar0 + ++nbar * G, D.status, &s_ok)) return;
     if (!resident) {
       griddep_launch();
       resident = true;
@@ -250,7 +461,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
       if (at < SW_CAND) W->cand[at] = k;
     }
   }
-  if (!sw_barrier(&W->bar, bar0 + ++nbar * G, D.status, &s_ok)) return;
+  if (!sw_barrier(W, bar0 + ++nbar * G, D.status, &s_ok)) return;
   if (!resident) griddep_launch();
   // every CTA has read the sums and appended its keys: clear a share of what
   // this launch used, and record where the next launch's barriers start
@@ -330,13 +541,21 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
 
 }  // namespace
 
+hs_status launch_select_token(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                              int32_t* d_topk, bool fp_keys, cudaStream_t st) {
+  if (n < 1) return HS_ERR_INVALID;
+  const int grid = n < num_sms() ? n : num_sms();
+  return launch_pdl(select_token_kernel, dim3(grid), dim3(SW_THREADS), 0, st, 0, p->d, scores, ld, d_limit, d_topk,
+                    n, fp_keys ? 1 : 0);
+}
+
 hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
-                             int32_t* d_topk, bool fp_keys, int G, bool hist0_done, cudaStream_t st) {
-  if (G < 1 || G > SW_MAX_G || n < 1 || n > p->d.sel_ws_tokens || n * G > num_sms() || (hist0_done && n != 1))
+                             int32_t* d_topk, bool fp_keys, int G, bool hist0_done, cudaStream_t st, bool withhold) {
+  if (G < 2 || G > SW_MAX_G || n < 1 || n > p->d.sel_ws_tokens || n * G > num_sms() || (hist0_done && n != 1))
     return HS_ERR_INVALID;
   if (ensure_kernel_attrs(select_wide_kernel, SW_SMEM) != HS_OK) return HS_ERR_CUDA;
   return launch_pdl(select_wide_kernel, dim3(n * G), dim3(SW_THREADS), SW_SMEM, st, 0, p->d, scores, ld, d_limit,
-                    d_topk, fp_keys ? 1 : 0, G, hist0_done ? 1 : 0);
+                    d_topk, fp_keys ? 1 : 0, G, hist0_done ? 1 : 0, withhold ? 1 : 0);
 }
 
 }  // namespace hs

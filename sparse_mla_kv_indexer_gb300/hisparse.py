@@ -16,8 +16,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhisparse
 STATUS = {
     0: "HS_OK", 1: "HS_ERR_INVALID", 2: "HS_ERR_OOM", 3: "HS_ERR_CAPACITY", 4: "HS_ERR_CUDA",
     5: "HS_ERR_TIMEOUT", 6: "HS_ERR_HOST_MISSING", 7: "HS_ERR_BAD_ID", 8: "HS_ERR_BAD_WEIGHT",
-    9: "HS_ERR_SCRATCH_LIMIT", 10: "HS_ERR_NOT_RESOLVED",
+    9: "HS_ERR_SCRATCH_LIMIT", 10: "HS_ERR_NOT_RESOLVED", 11: "HS_ERR_RANGE",
 }
+SELECT_AUTO, SELECT_LOCAL = 0, 1   # HS_SELECT_AUTO, HS_SELECT_LOCAL
 PLAN_PAD, PLAN_RESIDENT, PLAN_HIT, PLAN_MISS = 0, 1, 2, 3
 IDX_INT8, IDX_FP8 = 0, 1       # HS_IDX_INT8, HS_IDX_FP8
 IDX_FP8_PAGE_BYTES = 8448      # 64 x 128 e4m3 key bytes, then 64 fp32 scales
@@ -65,6 +66,8 @@ _SIGS = {
     "hs_sparse_mla_decode": [_P, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P],
     "hs_offload_pages": [_P, _I, _P, _P, _P],
     "hs_get_error": [_P, ctypes.POINTER(ctypes.c_int), _P],
+    "hs_set_select_mode": [_P, _I],
+    "hs_select_selftest": [_P, _I, _P, _P, _P],
     "hs_get_counters": [_P, ctypes.POINTER(Counters), _I, _P],
     "hs_link_probe": [_P, ctypes.c_int64, _I, _P, ctypes.c_int64, _P, _P],
     "hs_wait_selftest": [_P, _P],
@@ -213,6 +216,16 @@ class Pool:
         v = ctypes.c_int(0)
         _check("hs_get_error", lib.hs_get_error(self.handle, ctypes.byref(v), _stream(stream)))
         return v.value
+
+    def set_select_mode(self, mode: int) -> None:
+        """hs_set_select_mode: SELECT_LOCAL keeps the top-K selection off grid-wide waits."""
+        _check("hs_set_select_mode", lib.hs_set_select_mode(self.handle, mode))
+
+    def select_selftest(self, limit, topk, stream=None) -> None:
+        """hs_select_selftest: the grid-wide selection with one CTA per token withholding
+        its arrivals, so the others time out (HS_ERR_TIMEOUT, half-used scratch)."""
+        _check("hs_select_selftest", lib.hs_select_selftest(self.handle, limit.numel(), _ptr(limit), _ptr(topk),
+                                                            _stream(stream)))
 
     def wait_selftest(self, stream=None) -> None:
         """hs_wait_selftest: a bounded device wait that runs out (HS_ERR_TIMEOUT)."""

@@ -130,3 +130,73 @@ def test_host_side_checks_launch_nothing():
         assert pool.get_error() == 0                    # nothing reached the device
     finally:
         pool.close()
+
+
+def test_selection_wait_timeout_then_recovery_on_the_same_pool():
+    """The grid-wide top-K selection when one of its CTAs never arrives at a wait
+    (hs_select_selftest: as when another stream holds an SM): the others give up
+    after a second with HS_ERR_TIMEOUT and leave the token's scratch half used. The
+    next call on the same pool, before the error is read, still selects exactly what
+    the oracle selects (the scratch-free path); hs_get_error reports the timeout and
+    clears the scratch; the call after that takes the grid-wide path again and the
+    whole step (resolver, attention, page copies) matches the oracle. The local
+    selection mode (hs_set_select_mode) selects the same tokens."""
+    torch = _torch()
+    from oracle.engine import OracleRun
+    from sparse_mla_kv_indexer_gb300 import hisparse as H
+    from sparse_mla_kv_indexer_gb300 import schedule as S
+    from sparse_mla_kv_indexer_gb300 import workload as W
+    from sparse_mla_kv_indexer_gb300.driver import GpuRun
+    from test_gpu_parity import check_step
+    cfg = W.named_config("small_single")
+    wl = W.Workload(cfg)
+    sch = S.Schedule(cfg)
+    plans = [sch.plan(s) for s in range(2)]
+    oracle = OracleRun(wl, sch.setup)
+    gpu = GpuRun(wl, sch.setup)
+    try:
+        check_step(cfg, wl, plans[0], oracle.step(plans[0]), gpu.step(plans[0]), gpu, oracle, exact_scores=False)
+        o1 = oracle.step(plans[1])
+        gpu.apply_tick(plans[1].tick)
+        x = gpu.step_inputs(plans[1])
+        dev = gpu.dev
+        t = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in x.items() if k != "q_attn"}
+        gpu.pool.append_rows(t["app_req"], t["app_pos"], t["kv_rows"], t["idx_keys"])
+        n, K = len(plans[1].tokens), cfg.topk
+
+        def select():
+            out = torch.full((n, K), -7, dtype=torch.int32, device=dev)
+            gpu.pool.indexer_topk(0, t["req"], t["limit"], t["q_idx"][0], t["w_idx"][0], out)
+            torch.cuda.synchronize()
+            return out.cpu().numpy()
+
+        want = o1["topk"][0]
+        assert np.array_equal(select(), want)                  # grid-wide path, scores left in the pool
+        junk = torch.empty((n, K), dtype=torch.int32, device=dev)
+        gpu.pool.select_selftest(t["limit"], junk)              # one CTA per token withholds its arrivals
+        torch.cuda.synchronize()
+        assert np.array_equal(select(), want)                  # half-used scratch: routed around
+        assert gpu.pool.get_error() == TIMEOUT                 # reported once, scratch cleared
+        assert np.array_equal(select(), want)                  # grid-wide path again
+        assert gpu.pool.get_error() == 0
+        gpu.pool.set_select_mode(H.SELECT_LOCAL)
+        assert np.array_equal(select(), want)                  # no grid-wide waits at all
+        gpu.pool.set_select_mode(H.SELECT_AUTO)
+        with pytest.raises(H.HisparseError):
+            gpu.pool.set_select_mode(7)
+        # the rest of step 1 on the same pool, from its own selection
+        topk = torch.from_numpy(select()).to(dev)
+        rows = torch.empty_like(topk)
+        plan_t = torch.empty((n, K, 4), dtype=torch.int32, device=dev)
+        gpu.pool.resolve_topk(0, plans[1].step, t["req"], topk, rows, plan_t)
+        qa = torch.from_numpy(np.ascontiguousarray(x["q_attn"][0]).view(np.int16)).to(dev)
+        o = torch.empty((n, cfg.n_heads, 512), dtype=torch.int16, device=dev)
+        gpu.pool.sparse_mla_decode(0, qa, rows, wl.sm_scale(), o)
+        assert gpu.pool.get_error() == 0
+        assert np.array_equal(rows.cpu().numpy(), o1["row_ids"][0])
+        assert np.array_equal(plan_t.cpu().numpy()[..., 0], o1["kind"][0])
+        go = o.view(torch.bfloat16).float().cpu().numpy()
+        d = go - o1["o"][0]
+        assert np.abs(d).max() <= 1e-2 and np.linalg.norm(d) / np.linalg.norm(o1["o"][0]) <= 5e-3
+    finally:
+        gpu.close()
