@@ -209,7 +209,8 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
 
   if (warp >= SQ_GATHER_WARP0) {
     // ---------------------------------- gather ----------------------------------
-    const int gt = tid - SQ_GATHER_WARP0 * 32;
+    const int gt0 = tid - SQ_GATHER_WARP0 * 32;
+    const int gt = gt0;
     uint32_t it = 0;   // blocks this CTA has processed (the barrier phases)
     bool bad_range = false;
     for (int tok = blockIdx.x; tok < n_tok; tok += gridDim.x) {
@@ -252,13 +253,17 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
     if (c < SQ_CHUNKS) {                                                                     \
       const int r = c / ROW_CHUNKS, part = c - r * ROW_CHUNKS;                               \
       const int id = (BID)[r];                                                               \
-      if (id >= 0) rc[k] = __ldg(reinterpret_cast<const uint4*>(kv + (size_t)id * ROW) + part); \
+      if (id >= 0 && id < max_row) rc[k] = __ldg(reinterpret_cast<const uint4*>(kv + (size_t)id * ROW) + part); \
     }                                                                                        \
   }
       SQ_ISSUE(ids)
       bool failed = false;
       for (int b = 0; b < nb; ++b, ++it) {
+        int gt;   // opaque copy of the thread's index: the per-chunk rows and offsets are
+                  // recomputed each block instead of being kept in registers for the launch
+        asm volatile("mov.u32 %0, %1;" : "=r"(gt) : "r"(gt0));
         const bool okb = b == 0 || sq_wait(b_pv, (it - 1) & 1, D.status, dead);   // PV(b-1) has read the tile
+        asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's id copies (visible after the barrier)
         const int32_t* bid = ids + (b & 1) * ATTN_ROWS;
         // phase A: the rows' group scales (x 2^120) and the valid-row mask
 #pragma unroll
@@ -277,7 +282,9 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
           }
         }
         if (gt < ATTN_ROWS) {
-          const unsigned m = __ballot_sync(0xffffffffu, bid[gt] >= 0);
+          const int id = bid[gt];
+          if (id >= max_row) set_status(D.status, HS_ERR_BAD_ID);
+          const unsigned m = __ballot_sync(0xffffffffu, id >= 0 && id < max_row);
           if (lane == 0 && okb) vmask[gt >> 5] = m;
         }
         if (bar_any(1, SQ_GATHER, !okb)) {
@@ -309,16 +316,15 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
         fence_proxy_async();
         bar_named(1, SQ_GATHER);
         if (gt == 0) mbar_arrive1(b_tile);
-        // ids of block b+2 into the buffer block b's loads came from, then block b+1's loads
-        if (b + 2 < nb)
-          for (int i = gt; i < ATTN_ROWS; i += SQ_GATHER) {
-            int id = __ldg(rid + (b + 2) * ATTN_ROWS + i);
-            if (id >= max_row) {
-              set_status(D.status, HS_ERR_BAD_ID);
-              id = -1;
-            }
-            ids[(b & 1) * ATTN_ROWS + i] = id;
-          }
+        // ids of block b+2 into the buffer block b's loads came from, by asynchronous
+        // copies (no thread waits for them here; they are checked when used), then
+        // block b+1's loads
+        if (b + 2 < nb && gt < ATTN_ROWS) {
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(ids + (b & 1) * ATTN_ROWS + gt)),
+                       "l"(rid + (b + 2) * ATTN_ROWS + gt)
+                       : "memory");
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        }
         if (b + 1 < nb) {
           const int32_t* nid = ids + ((b + 1) & 1) * ATTN_ROWS;
           SQ_ISSUE(nid)
@@ -383,36 +389,53 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
         const bool okb = sq_wait(b_s, it & 1, D.status, dead);
         tc_fence_after();
         const bool valid = (vmask[row >> 5] >> (row & 31)) & 1u;
-        // block maximum per head, one half of the heads at a time (the reduction
-        // consumes its registers; S is read again from TMEM for the exponentials)
+        // Does any row exceed a head's reference maximum by more than the lazy bound?
+        // Usually not after the first block: then the block maximum is not needed.
+        bool over = false;
 #pragma unroll
         for (int hh = 0; hh < 64; hh += 32) {
-          float t[32];
-          tmem_ld32(lane_base + SQ_TM_S + hh, *reinterpret_cast<uint32_t(*)[32]>(t));
+          uint32_t t[32];
+          tmem_ld32(lane_base + SQ_TM_S + hh, t);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) t[h] = valid ? __uint_as_float(__float_as_uint(t[h])) * scale_log2 : -INFINITY;
-          red[warp * 64 + hh + lane] = warp_reduce32<true>(t);
+          for (int h = 0; h < 32; ++h) over |= valid && __uint_as_float(t[h]) * scale_log2 > mref[hh + h] + SQ_RESCALE_LOG2;
         }
         if (bar_any(2, 128, !okb)) {   // the role stops as one when a wait ran out
           failed = true;
           break;
         }
-        if (tid < SQ_H) {
-          const float bm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
-          const float mo = mref[tid];
-          float f = 1.f;
-          if (bm > -INFINITY && (mo == -INFINITY || bm > mo + SQ_RESCALE_LOG2)) {
-            if (mo != -INFINITY) {
-              f = exp2f(mo - bm);
-              *f_rescale = 1;
-            }
-            mref[tid] = bm;
+        const bool need_max = bar_any(2, 128, over);
+        if (need_max) {
+          // block maximum per head, one half of the heads at a time (the reduction
+          // consumes its registers; S is read again from TMEM for the exponentials)
+#pragma unroll
+          for (int hh = 0; hh < 64; hh += 32) {
+            float t[32];
+            tmem_ld32(lane_base + SQ_TM_S + hh, *reinterpret_cast<uint32_t(*)[32]>(t));
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) t[h] = valid ? t[h] * scale_log2 : -INFINITY;
+            red[warp * 64 + hh + lane] = warp_reduce32<true>(t);
           }
-          fac[tid] = f;
+          bar_named(2, 128);
+          if (tid < SQ_H) {
+            const float bm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+            const float mo = mref[tid];
+            float f = 1.f;
+            if (bm > -INFINITY && (mo == -INFINITY || bm > mo + SQ_RESCALE_LOG2)) {
+              if (mo != -INFINITY) {
+                f = exp2f(mo - bm);
+                *f_rescale = 1;
+              }
+              mref[tid] = bm;
+            }
+            fac[tid] = f;
+          }
+          bar_named(2, 128);
+        } else if (tid < SQ_H) {
+          fac[tid] = 1.f;   // read only by this thread below (no rescale this block)
         }
-        bar_named(2, 128);
-        const bool rescale = *f_rescale != 0;
+        const bool rescale = need_max && *f_rescale != 0;
         float p[64];   // p = 2^(z - m)
         tmem_ld32(lane_base + SQ_TM_S, *reinterpret_cast<uint32_t(*)[32]>(p));
         tmem_ld32(lane_base + SQ_TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(p + 32));

@@ -181,13 +181,16 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, const __grid
   const uint32_t tmem = *tmem_slot;
   const int nseg = *s_nseg;
   const int total = nseg ? segs[nseg - 1].tile_end : 0;
-  // Each CTA takes a contiguous run of tiles: in a batch of requests a CTA then meets
+  // With several requests each CTA takes a contiguous run of tiles: a CTA then meets
   // one or two request boundaries in the whole launch, and each boundary drains its
   // pipeline (the query operand and the head weights of the next request are loaded
-  // once the previous request's MMAs and epilogues are done).
+  // once the previous request's MMAs and epilogues are done). A single request is
+  // dealt round robin, which measured faster (the CTAs sweep the keys together).
+  const bool runs = nseg > 1;
   const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int first_item = (int)blockIdx.x * per;
-  const int n_local = total > first_item ? min(per, total - first_item) : 0;
+  const int first_item = runs ? (int)blockIdx.x * per : (int)blockIdx.x;
+  const int n_local = runs ? (total > first_item ? min(per, total - first_item) : 0)
+                           : (total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0);
   auto seg_of = [&](int item) {
     int lo = 0, hi = nseg - 1;
     while (lo < hi) {
@@ -196,7 +199,7 @@ indexer_fp8_kernel(Dev D, const __grid_constant__ CUtensorMap tmap, const __grid
     }
     return lo;
   };
-  auto item_of = [&](int i) { return first_item + i; };
+  auto item_of = [&](int i) { return runs ? first_item + i : first_item + i * (int)gridDim.x; };
 
   if (warp == F8_PRODUCER_WARP) {
     // ------------------------------ producer ------------------------------

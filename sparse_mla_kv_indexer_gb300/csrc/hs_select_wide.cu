@@ -102,18 +102,17 @@ __device__ __forceinline__ bool in_range(unsigned long long k, unsigned long lon
 }
 
 // ---- one CTA selects the top K of one token, streaming its keys from global memory ----
-// Warp w owns a contiguous range of the token's keys (a multiple of 512 keys, so
-// every lane reads 16 keys with eight 16-byte loads, all in flight at once), so the
+// Warp w owns a contiguous range of the token's keys (a multiple of 32 x ST_PER_LANE
+// keys, each lane reading its keys with 16-byte loads, all in flight at once), so the
 // emit pass can write its selected tokens in ascending order at a known offset.
 // Passes over the keys (reads from L2): the level-0 histogram, further histogram
 // levels while the range holding the K-th largest key has more than SW_CAND keys,
 // the collection of that range (each warp also counts its keys above it), and the
 // emit pass.
-constexpr int ST_PER_LANE = 16;
-constexpr int ST_SPAN = 32 * ST_PER_LANE;   // keys per warp step
 
-// The ST_PER_LANE keys of a lane at i (a multiple of 16); keys at or beyond `hi` are 0 and
+// The ST_PER_LANE keys of a lane at i (a multiple of ST_PER_LANE); keys at or beyond `hi` are 0 and
 // flagged invalid (bit k of the returned mask set for a valid key k).
+template <int ST_PER_LANE>
 __device__ __forceinline__ uint32_t st_load_lane(const long long* s, int i, int hi,
                                                 unsigned long long (&k)[ST_PER_LANE], int32_t* status) {
   longlong2 v[ST_PER_LANE / 2];
@@ -136,10 +135,15 @@ __device__ __forceinline__ uint32_t st_load_lane(const long long* s, int i, int 
   return valid;
 }
 
+// ST_PER_LANE keys per lane in flight: 8 for the many-token selection (measured best of
+// 4, 8 and 16 at 32 requests x 4 tokens); the recovery
+// path inside the grid-wide kernel takes 4, which keeps that kernel's registers low.
+template <int ST_PER_LANE>
 __device__ void select_token_cta(const long long* __restrict__ s, int n, int K, bool fp_keys, int32_t* __restrict__ out,
                                  int32_t* status, uint32_t* hist, unsigned long long* cand, int* warp_tot,
                                  int* s_small) {
   constexpr int NW = SW_THREADS / 32;
+  constexpr int ST_SPAN = 32 * ST_PER_LANE;   // keys per warp step
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int* s_bin = s_small;
   int* s_cnt = s_small + 1;
@@ -247,7 +251,7 @@ __device__ void select_token_cta(const long long* __restrict__ s, int n, int K, 
     }
   }
   __syncthreads();
-  // emit: the lanes of a warp hold 16 consecutive keys each, so a lane's selected keys
+  // emit: the lanes of a warp hold ST_PER_LANE consecutive keys each, so a lane's selected keys
   // follow those of the lanes before it
   int wbase = w_off[wid];
   for (int i0 = wlo; i0 < whi; i0 += ST_SPAN) {
@@ -287,7 +291,7 @@ select_token_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int
   for (int tok = blockIdx.x; tok < n_tok; tok += gridDim.x) {
     int n = limit_of[tok];
     n = max(0, min(n, D.max_ctx));
-    select_token_cta(reinterpret_cast<const long long*>(scores) + (size_t)tok * ld, n, D.topk, fp_keys != 0,
+    select_token_cta<8>(reinterpret_cast<const long long*>(scores) + (size_t)tok * ld, n, D.topk, fp_keys != 0,
                      topk + (size_t)tok * D.topk, D.status, hist, cand, warp_tot, s_small);
     __syncthreads();
   }
@@ -329,7 +333,7 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
     // token is selected by its first CTA alone, without the scratch and without waits.
     griddep_launch();
     if (g == 0)
-      select_token_cta(reinterpret_cast<const long long*>(scores) + (size_t)tok * ld, n, K, fp_keys != 0, out,
+      select_token_cta<4>(reinterpret_cast<const long long*>(scores) + (size_t)tok * ld, n, K, fp_keys != 0, out,
                        D.status, hist, cand, warp_tot, dirty_small);
     return;
   }
