@@ -12,7 +12,8 @@
 // spreads one token over more SMs and shortens every per-CTA phase after the
 // gather (each head group gathers the same rows; the repeats hit L2).
 //  * every thread loads ~10 of the block's 16-byte row chunks at once, gathered by
-//    HMA row id (one stride for resident and hot rows), and puts each chunk in
+//    HMA row id (one stride for resident and hot rows; chunks dealt by row_piece so
+//    that the stores of one shared-memory cycle hit distinct banks), and puts each chunk in
 //    place: the FP8 latent widened to bf16 by a bit shuffle that is exact up to
 //    the constant factor 2^-120 (normal and subnormal e4m3 alike), the fp32 group
 //    scales to a small table, the bf16 rope unchanged; the 128 x 576 bf16 tile
@@ -195,7 +196,8 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
     const int c = tid + k * AT_THREADS;
     rc[k] = make_uint4(0, 0, 0, 0);
     if (c < AT_CHUNKS) {
-      const int r = c / ROW_CHUNKS, part = c - r * ROW_CHUNKS;
+      int r, part;
+      row_piece(c, r, part);
       const int id = ids[r];
       if (id >= 0) {
         const uint4* src = reinterpret_cast<const uint4*>(kv + (size_t)id * ROW) + part;
@@ -215,7 +217,8 @@ attention_kernel(Dev D, int layer, const uint16_t* __restrict__ q, const int32_t
   for (int k = 0; k < AT_CPT; ++k) {
     const int c = tid + k * AT_THREADS;
     if (c < AT_CHUNKS) {
-      const int r = c / ROW_CHUNKS, part = c - r * ROW_CHUNKS;
+      int r, part;
+      row_piece(c, r, part);
       const uint4 v = rc[k];
       if (part < 32) {            // 16 latent bytes = dims 16 part .. 16 part + 15
         const uint2 a = e4m3x4_to_bf16x4_scaled(v.x), b = e4m3x4_to_bf16x4_scaled(v.y);

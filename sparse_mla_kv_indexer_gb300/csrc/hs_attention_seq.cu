@@ -18,7 +18,8 @@
 //   warps 5-15  gather: the 128 rows of a block, by HMA row id, 16 bytes per load,
 //               into registers one block ahead; then the fp16 operand tile
 // Per block b of 128 rows:
-//   gather   wait until PV(b-1) has read the tile; write the tile: latent values
+//   gather   wait until PV(b-1) has read the tile; write the tile (pieces dealt so
+//            that stores of one shared-memory cycle hit distinct banks): latent values
 //            e4m3 x group scale rounded once to fp16, rope bf16 -> fp16 (exact);
 //            then issue the loads of block b+1
 //   MMA      S = K_b . Q^T (M = 128 rows, N = 64 heads, K = 576) into TMEM
@@ -251,7 +252,8 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
     const int c = gt + k * SQ_GATHER;                                                        \
     rc[k] = make_uint4(0, 0, 0, 0);                                                          \
     if (c < SQ_CHUNKS) {                                                                     \
-      const int r = c / ROW_CHUNKS, part = c - r * ROW_CHUNKS;                               \
+      int r, part;                                                                           \
+      row_piece(c, r, part);                                                                  \
       const int id = (BID)[r];                                                               \
       if (id >= 0 && id < max_row) rc[k] = __ldg(reinterpret_cast<const uint4*>(kv + (size_t)id * ROW) + part); \
     }                                                                                        \
@@ -270,7 +272,8 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
         for (int k = 0; k < SQ_CPT; ++k) {
           const int c = gt + k * SQ_GATHER;
           if (c < SQ_CHUNKS) {
-            const int r = c / ROW_CHUNKS, part = c - r * ROW_CHUNKS;
+            int r, part;
+            row_piece(c, r, part);
             if (part == 32) {
               const float4 s = make_float4(__uint_as_float(rc[k].x), __uint_as_float(rc[k].y),
                                            __uint_as_float(rc[k].z), __uint_as_float(rc[k].w));
@@ -296,7 +299,8 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
         for (int k = 0; k < SQ_CPT; ++k) {
           const int c = gt + k * SQ_GATHER;
           if (c < SQ_CHUNKS) {
-            const int r = c / ROW_CHUNKS, part = c - r * ROW_CHUNKS;
+            int r, part;
+            row_piece(c, r, part);
             const uint4 v = rc[k];
             if (part < 32) {   // latent dims 16 part .. 16 part + 15, group part / 8
               const float4 s4 = scl[r];

@@ -387,6 +387,30 @@ __host__ __device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
   return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
 }
 
+// The 5,248 16-byte pieces of a 128-row attention block (128 rows x 41 parts), in the
+// order the gathering threads of a CTA take them (slot c goes to thread c % threads,
+// a multiple of 32): the row and the 16-byte part of the 656-byte row it holds. Every group of 8 consecutive slots (8 threads that store in
+// one shared-memory cycle) covers 4 parts of two rows whose swizzled 16-byte slots
+// differ, so the group's 16-byte stores of the fp16 tile fall on 8 different bank
+// groups, and a warp's loads cover two runs of 256 contiguous bytes.
+//   slots [0, 4096)     latent parts 0-31: rows 2P, 2P + 1 (P = c / 64), parts 4j .. 4j + 3
+//   slots [4096, 5120)  rope parts 33-40: rows 8G + q and 8G + q + 4, four parts each
+//   slots [5120, 5248)  part 32 (the four group scales) of row c - 5120
+__host__ __device__ __forceinline__ void row_piece(int c, int& r, int& part) {
+  if (c < 4096) {
+    const int u = c >> 3, t = c & 7;
+    r = 2 * (u >> 3) + (t >> 2);
+    part = 4 * (u & 7) + (t & 3);
+  } else if (c < 5120) {
+    const int u = (c - 4096) >> 3, t = c & 7;
+    r = 8 * (u >> 3) + ((u >> 1) & 3) + 4 * (t >> 2);
+    part = 33 + 4 * (u & 1) + (t & 3);
+  } else {
+    r = c - 5120;
+    part = 32;
+  }
+}
+
 // ---- programmatic dependent launch -------------------------------------------------
 // A hot-path kernel may start while its predecessor in the stream finishes; it
 // runs its address-independent prologue, then waits for the predecessor's
