@@ -329,26 +329,20 @@ def sources_sha256(files):
     return h.hexdigest()
 
 
-def ncu_traffic(kernel_files, name, workload):
-    """DRAM bytes per launch of call `name` on `workload` from a committed ncu summary,
-    if taken on the current sources."""
+def ncu_traffic(name, workload):
+    """DRAM bytes (read + write) per call of `name` on `workload`: the sum over the call's
+    kernels of one single-kernel ncu capture each, committed with the sha256 of the kernel
+    sources it was taken on; None when there is no capture or a source has changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         ent = d[name + "@" + workload]
-        if ent.get("source_sha256") != sources_sha256(kernel_files):
+        if ent.get("source_sha256") != sources_sha256(ent["sources"]):
             return None
         return ent.get("bytes_per_launch")
     except Exception:
         return None
-
-
-# the sources of each call's kernels (their sha256 keys the committed ncu traffic)
-KERNEL_FILES = {"indexer_topk": ["hs_indexer.cu", "hs_select.cuh", "hs_select_wide.cu"],
-                "indexer_topk_fp8": ["hs_indexer_fp8.cu", "hs_select.cuh", "hs_select_wide.cu"],
-                "sparse_mla_decode": ["hs_attention.cu"], "resolve_topk": ["hs_resolver.cu"],
-                "offload_pages": ["hs_pool.cu"], "append": ["hs_pool.cu"]}
 
 
 # ---------------------------------------------------------------------------
@@ -613,7 +607,7 @@ def measure(args, name, K, Wm, rank, world, local, cpu_baseline):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes,
-                     "traffic": ncu_traffic(KERNEL_FILES.get(tkey, []), tkey, name)},
+                     "traffic": ncu_traffic(tkey, name)},
         "step_roofline": {"algorithmic_hbm_bytes": step_bytes, "miss_bytes": miss_bytes,
                           "host_link_gbs": link["single_row_gbs"], "tensor_flops": flops,
                           "tensor_peak_tflops": tflops, "tensor_peak_source": tflops_kind,
