@@ -25,18 +25,23 @@
 //   MMA      S = K_b . Q^T (M = 128 rows, N = 64 heads, K = 576) into TMEM
 //   softmax  z = S * sm_scale * log2(e); per-head running maximum with a lazy
 //            rescale (the reference maximum moves only when a block's maximum
-//            exceeds it by more than 2^8, and then O and the running sum are
-//            rescaled in place); P = 2^(z - m) in fp16 into the tile's rope columns,
-//            which QK(b) no longer needs; running sum per head
+//            exceeds it by more than 2^8, and then O and l are rescaled in place);
+//            P = 2^(z - m) in fp16 into the tile's rope columns, which QK(b) no
+//            longer needs
 //   MMA      O^T += V_b^T . P^T per 128-dim group (M = 128 dims, N = 64 heads,
-//            K = 128 rows), O in TMEM for the whole token
+//            K = 128 rows), O in TMEM for the whole token; and l += 1 . P^T, the
+//            running sum of P per head, with an all-ones A operand held in TMEM
+//            (every TMEM lane of l then holds the sums of all heads)
 // After the last block: out = O / l in bf16, lse = m + log(l).
 //
 // Precision: the scale of each 128-value group is folded into the fp16 operand
-// (one rounding, relative 2^-11), so one accumulator holds the whole score; P is
+// (the exact e4m3 value times the scale rounded to fp16, relative error within 2^-10),
+// so one accumulator holds the whole score; P is
 // fp16; accumulation is fp32. fp16 bounds the inputs: |group scale| < 146 (so
 // 448 x scale < 65504), and the query and rope values below 65504 in magnitude;
 // values outside set HS_ERR_RANGE. Every wait is bounded (HS_ERR_TIMEOUT).
+#include <cuda_fp8.h>
+
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -58,12 +63,10 @@ constexpr int SQ_QCHUNKS = SQ_H * 72;                                         //
 constexpr int SQ_QCPT = (SQ_QCHUNKS + SQ_GATHER - 1) / SQ_GATHER;             // 14
 // misc region
 constexpr int SQ_M_IDS = 0;                        // int32 [2][128]
-constexpr int SQ_M_SCL = SQ_M_IDS + 2 * 128 * 4;   // float4 [128]: group scales x 2^120
+constexpr int SQ_M_SCL = SQ_M_IDS + 2 * 128 * 4;   // float4 [128]: the rows' four group scales
 constexpr int SQ_M_RED = SQ_M_SCL + 128 * 16;      // float [4][64] block maximum per warp
-constexpr int SQ_M_RED2 = SQ_M_RED + 4 * 64 * 4;   // float [4][64] block sum per warp
-constexpr int SQ_M_MREF = SQ_M_RED2 + 4 * 64 * 4;  // float [64] reference maximum (log2 units)
-constexpr int SQ_M_LRUN = SQ_M_MREF + 64 * 4;      // float [64] running sum
-constexpr int SQ_M_FAC = SQ_M_LRUN + 64 * 4;       // float [64] rescale factor of this block
+constexpr int SQ_M_MREF = SQ_M_RED + 4 * 64 * 4;   // float [64] reference maximum (log2 units)
+constexpr int SQ_M_FAC = SQ_M_MREF + 64 * 4;       // float [64] rescale factor of this block
 constexpr int SQ_M_VMASK = SQ_M_FAC + 64 * 4;      // uint32 [4] valid rows of the block
 constexpr int SQ_M_FLAGS = SQ_M_VMASK + 16;        // int32 [4]: rescale, dead
 constexpr int SQ_M_BAR = SQ_M_FLAGS + 16;          // uint64 [5]: tile_full, s_full, p_full, pv_done, fin
@@ -74,6 +77,9 @@ static_assert(SQ_SMEM <= 232448, "shared memory budget");
 static_assert(SQ_CPT * SQ_GATHER >= SQ_CHUNKS && SQ_QCPT * SQ_GATHER >= SQ_QCHUNKS, "chunk cover");
 constexpr uint32_t SQ_TM_O = 0;     // O^T: 4 accumulators of 64 columns (128 dims x 64 heads)
 constexpr uint32_t SQ_TM_S = 256;   // S: 128 rows x 64 heads
+constexpr uint32_t SQ_TM_L = 320;   // l: 64 columns, the running sum of each head (same in every lane)
+constexpr uint32_t SQ_TM_ONE = 384; // all-ones fp16 A operand of the l MMA (8 columns per 16 rows of K;
+                                    // columns 384-511 are all filled with ones)
 constexpr float SQ_LOG2E = 1.4426950408889634f;
 constexpr float SQ_TWO_POW_120 = 1.329227995784916e36f;
 constexpr float SQ_RESCALE_LOG2 = 8.f;   // lazy rescale threshold: p <= 2^8
@@ -105,6 +111,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// D[tmem] (+)= A . B (kind::f16) with the A operand read from tensor memory.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
@@ -118,6 +138,16 @@ __device__ __forceinline__ uint2 e4m3x4_scaled_f16(uint32_t w, float s120) {
   const float f2 = __uint_as_float(((w & 0x800000u) << 8) | ((w & 0x7F0000u) << 4));
   const float f3 = __uint_as_float((w & 0x80000000u) | ((w & 0x7F000000u) >> 4));
   return make_uint2(h2_bits(__floats2half2_rn(f0 * s120, f1 * s120)), h2_bits(__floats2half2_rn(f2 * s120, f3 * s120)));
+}
+
+// Four e4m3 bytes times a group scale in fp16: the hardware conversion of each e4m3
+// pair to fp16 (exact), then one fp16 multiply per pair by the scale rounded to fp16
+// (two roundings, relative error within 2^-10). Used when the scale is a normal fp16
+// value (>= 2^-14), else e4m3x4_scaled_f16.
+__device__ __forceinline__ uint2 e4m3x4_times_f16(uint32_t w, __half2 s2) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  return make_uint2(h2_bits(__hmul2(__half2(lo), s2)), h2_bits(__hmul2(__half2(hi), s2)));
 }
 
 // Eight bf16 values -> eight fp16 (exact inside the fp16 range); *bad is set when a
@@ -177,9 +207,7 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
   int32_t* ids = reinterpret_cast<int32_t*>(misc + SQ_M_IDS);
   float4* scl = reinterpret_cast<float4*>(misc + SQ_M_SCL);
   float* red = reinterpret_cast<float*>(misc + SQ_M_RED);
-  float* red2 = reinterpret_cast<float*>(misc + SQ_M_RED2);
   float* mref = reinterpret_cast<float*>(misc + SQ_M_MREF);
-  float* lrun = reinterpret_cast<float*>(misc + SQ_M_LRUN);
   float* fac = reinterpret_cast<float*>(misc + SQ_M_FAC);
   uint32_t* vmask = reinterpret_cast<uint32_t*>(misc + SQ_M_VMASK);
   volatile int32_t* f_rescale = reinterpret_cast<int32_t*>(misc + SQ_M_FLAGS);
@@ -279,8 +307,7 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
                                            __uint_as_float(rc[k].z), __uint_as_float(rc[k].w));
               bad_range |= !(fabsf(s.x) < SQ_MAX_SCALE && fabsf(s.y) < SQ_MAX_SCALE && fabsf(s.z) < SQ_MAX_SCALE &&
                              fabsf(s.w) < SQ_MAX_SCALE);
-              scl[r] = make_float4(s.x * SQ_TWO_POW_120, s.y * SQ_TWO_POW_120, s.z * SQ_TWO_POW_120,
-                                   s.w * SQ_TWO_POW_120);
+              scl[r] = s;
             }
           }
         }
@@ -306,8 +333,16 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
               const float4 s4 = scl[r];
               const int g = part >> 3;
               const float s = g == 0 ? s4.x : g == 1 ? s4.y : g == 2 ? s4.z : s4.w;
-              const uint2 a = e4m3x4_scaled_f16(v.x, s), bq = e4m3x4_scaled_f16(v.y, s);
-              const uint2 cq = e4m3x4_scaled_f16(v.z, s), d = e4m3x4_scaled_f16(v.w, s);
+              uint2 a, bq, cq, d;
+              if (fabsf(s) >= 6.103515625e-05f) {   // 2^-14: a normal fp16 scale
+                const __half2 s2 = __float2half2_rn(s);
+                a = e4m3x4_times_f16(v.x, s2), bq = e4m3x4_times_f16(v.y, s2);
+                cq = e4m3x4_times_f16(v.z, s2), d = e4m3x4_times_f16(v.w, s2);
+              } else {
+                const float s120 = s * SQ_TWO_POW_120;
+                a = e4m3x4_scaled_f16(v.x, s120), bq = e4m3x4_scaled_f16(v.y, s120);
+                cq = e4m3x4_scaled_f16(v.z, s120), d = e4m3x4_scaled_f16(v.w, s120);
+              }
               uint8_t* col = tile + (part >> 2) * SQ_COL;
               const int chunk = (part & 3) * 2;
               *reinterpret_cast<uint4*>(col + sw128_chunk(r, chunk)) = make_uint4(a.x, a.y, bq.x, bq.y);
@@ -344,6 +379,7 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
       uint32_t it = 0;
       const uint32_t idesc_qk = idesc_f16(128, SQ_H, false, false, false);
       const uint32_t idesc_pv = idesc_f16(128, SQ_H, true, true, false);
+      const uint32_t idesc_l = idesc_f16(128, SQ_H, false, true, false);
       const uint32_t t0 = smem_u32(tile), q0 = smem_u32(Qs), p0 = smem_u32(Ps);
       bool failed = false;
       for (int tok = blockIdx.x; tok < n_tok && !failed; tok += gridDim.x) {
@@ -373,6 +409,10 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
               const uint64_t bd = smem_desc_sw128(p0 + kk * 2048, SQ_COL, 1024);
               umma_f16(tmem + SQ_TM_O + g * 64, ad, bd, idesc_pv, (b > 0 || kk > 0) ? 1u : 0u);
             }
+#pragma unroll
+          for (int kk = 0; kk < ATTN_ROWS / 16; ++kk)
+            umma_f16_ta(tmem + SQ_TM_L, tmem + SQ_TM_ONE + kk * 8, smem_desc_sw128(p0 + kk * 2048, SQ_COL, 1024),
+                        idesc_l, (b > 0 || kk > 0) ? 1u : 0u);
           umma_commit(b_pv);
         }
       }
@@ -381,13 +421,20 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
     // ---------------------------------- softmax and output ----------------------------------
     const int row = tid;   // 0..127: TMEM lane and tile row
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float4* mref4 = reinterpret_cast<const float4*>(mref);
+    {   // the all-ones operand of the l MMA (fp16 1.0 pairs); made visible to the MMA
+        // warp by the fences and the barrier before the first P hand-off
+      uint32_t one[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) one[j] = 0x3C003C00u;
+#pragma unroll
+      for (int c = 0; c < 512 - SQ_TM_ONE; c += 32) tmem_st32(lane_base + SQ_TM_ONE + c, one);
+      tmem_wait_st();
+    }
     uint32_t it = 0;
     bool failed = false;
     for (int tok = blockIdx.x; tok < n_tok && !failed; tok += gridDim.x) {
-      if (tid < SQ_H) {
-        mref[tid] = -INFINITY;
-        lrun[tid] = 0.f;
-      }
+      if (tid < SQ_H) mref[tid] = -INFINITY;
       bar_named(2, 128);
       for (int b = 0; b < nb; ++b, ++it) {
         const bool okb = sq_wait(b_s, it & 1, D.status, dead);
@@ -402,13 +449,19 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
           tmem_ld32(lane_base + SQ_TM_S + hh, t);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) over |= valid && __uint_as_float(t[h]) * scale_log2 > mref[hh + h] + SQ_RESCALE_LOG2;
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 m4 = mref4[hh / 4 + h4];
+            over |= __uint_as_float(t[4 * h4]) * scale_log2 > m4.x + SQ_RESCALE_LOG2;
+            over |= __uint_as_float(t[4 * h4 + 1]) * scale_log2 > m4.y + SQ_RESCALE_LOG2;
+            over |= __uint_as_float(t[4 * h4 + 2]) * scale_log2 > m4.z + SQ_RESCALE_LOG2;
+            over |= __uint_as_float(t[4 * h4 + 3]) * scale_log2 > m4.w + SQ_RESCALE_LOG2;
+          }
         }
         if (bar_any(2, 128, !okb)) {   // the role stops as one when a wait ran out
           failed = true;
           break;
         }
-        const bool need_max = bar_any(2, 128, over);
+        const bool need_max = bar_any(2, 128, over && valid);
         if (need_max) {
           // block maximum per head, one half of the heads at a time (the reduction
           // consumes its registers; S is read again from TMEM for the exponentials)
@@ -436,8 +489,6 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
             fac[tid] = f;
           }
           bar_named(2, 128);
-        } else if (tid < SQ_H) {
-          fac[tid] = 1.f;   // read only by this thread below (no rescale this block)
         }
         const bool rescale = need_max && *f_rescale != 0;
         float p[64];   // p = 2^(z - m)
@@ -445,11 +496,16 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
         tmem_ld32(lane_base + SQ_TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(p + 32));
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 64; ++h) {
-          const float m = mref[h];
-          p[h] = (!valid || m == -INFINITY) ? 0.f : exp2f(p[h] * scale_log2 - m);
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 m4 = mref4[h4];
+          const float m[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int h = 4 * h4 + k;
+            p[h] = (!valid || m[k] == -INFINITY) ? 0.f : ex2_approx(p[h] * scale_log2 - m[k]);
+          }
         }
-        // P^T row: 64 heads in one 128-byte line (MN-major B operand of PV)
+        // P^T row: 64 heads in one 128-byte line (MN-major B operand of PV and of l)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const float* pp = p + 8 * c;
@@ -457,31 +513,24 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
               make_uint4(h2_bits(__floats2half2_rn(pp[0], pp[1])), h2_bits(__floats2half2_rn(pp[2], pp[3])),
                          h2_bits(__floats2half2_rn(pp[4], pp[5])), h2_bits(__floats2half2_rn(pp[6], pp[7])));
         }
-        {
-          const float s0 = warp_reduce32<false>(*reinterpret_cast<float(*)[32]>(p));
-          const float s1 = warp_reduce32<false>(*reinterpret_cast<float(*)[32]>(p + 32));
-          red2[warp * 64 + lane] = s0;
-          red2[warp * 64 + 32 + lane] = s1;
-        }
-        if (rescale) {   // a block raised some head's maximum by more than 2^8: O *= 2^(m_old - m_new)
+        if (rescale) {   // a block raised some head's maximum by more than 2^8: O, l *= 2^(m_old - m_new)
 #pragma unroll 1
-          for (int g = 0; g < 4; ++g)
+          for (int g = 0; g < 5; ++g)
 #pragma unroll 1
             for (int hh = 0; hh < 64; hh += 32) {
+              const uint32_t col = (g < 4 ? SQ_TM_O + g * 64 : SQ_TM_L) + hh;
               uint32_t o[32];
-              tmem_ld32(lane_base + SQ_TM_O + g * 64 + hh, o);
+              tmem_ld32(lane_base + col, o);
               tmem_wait_ld();
 #pragma unroll
               for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * fac[hh + j]);
-              tmem_st32(lane_base + SQ_TM_O + g * 64 + hh, o);
+              tmem_st32(lane_base + col, o);
             }
           tmem_wait_st();
         }
         fence_proxy_async();
         tc_fence_before();
         bar_named(2, 128);
-        if (tid < SQ_H)
-          lrun[tid] = lrun[tid] * fac[tid] + (red2[tid] + red2[64 + tid]) + (red2[128 + tid] + red2[192 + tid]);
         if (tid == 0) {
           *f_rescale = 0;
           mbar_arrive1(b_p);
@@ -490,29 +539,36 @@ attention_seq_kernel(Dev D, int layer, int n_tok, const uint16_t* __restrict__ q
       if (failed) break;
       const bool okl = sq_wait(b_pv, (it - 1) & 1, D.status, dead);
       tc_fence_after();
-      if (bar_any(2, 128, !okl)) break;   // lrun final
-      // out[tok][h][128 g + t] = O_g[t][h] / l[h]
+      if (bar_any(2, 128, !okl)) break;
+      // out[tok][h][128 g + t] = O_g[t][h] / l[h]; this thread's lane of l holds every head
       uint16_t* ot = out + (size_t)tok * SQ_H * 512 + warp * 32 + lane;
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g)
+      for (int hh = 0; hh < 64; hh += 32) {
+        uint32_t l[32];
+        tmem_ld32(lane_base + SQ_TM_L + hh, l);
+        tmem_wait_ld();
 #pragma unroll 1
-        for (int hh = 0; hh < 64; hh += 32) {
+        for (int g = 0; g < 4; ++g) {
           uint32_t o[32];
           tmem_ld32(lane_base + SQ_TM_O + g * 64 + hh, o);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float l = lrun[hh + j];
+            const float lj = __uint_as_float(l[j]);
             ot[(size_t)(hh + j) * 512 + g * 128] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(l > 0.f ? __uint_as_float(o[j]) / l : 0.f));
+                __bfloat16_as_ushort(__float2bfloat16_rn(lj > 0.f ? __uint_as_float(o[j]) / lj : 0.f));
           }
         }
-      if (lse_out && tid < SQ_H) {
-        const float l = lrun[tid];
-        lse_out[(size_t)tok * SQ_H + tid] = l > 0.f ? (mref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        if (lse_out && warp == (hh >> 5)) {   // warp 0 the heads 0-31, warp 1 the heads 32-63
+          float lh = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) lh = j == lane ? __uint_as_float(l[j]) : lh;
+          const int h = hh + lane;
+          lse_out[(size_t)tok * SQ_H + h] = lh > 0.f ? (mref[h] + log2f(lh)) * 0.6931471805599453f : -INFINITY;
+        }
       }
       tc_fence_before();
-      bar_named(2, 128);   // every O read and lrun read before the next token's first PV and init
+      bar_named(2, 128);   // every O and l read before the next token's first PV and init
     }
   }
   __syncthreads();
