@@ -220,7 +220,11 @@ hs_status hs_append_rows(hs_pool* pool, int32_t n_tokens, const int32_t* d_req,
  * that holds SMs for longer than the one-second wait limit makes the call fail with
  * HS_ERR_TIMEOUT (read by hs_get_error, which also clears the selection scratch the
  * timed-out call left). hs_set_select_mode(pool, HS_SELECT_LOCAL) avoids this path
- * for engines that share the GPU; the no-allocation variant below never uses it. */
+ * for engines that share the GPU; the no-allocation variant below never uses it.
+ * With many query tokens (up to one per SM) each token's scores are cut into chunks
+ * spread over the GPU with no cross-CTA waits; beyond that, one CTA per token. The
+ * chunked path keeps about 65 KB of scratch per query token of the pool (max_tokens) and,
+ * like the wide one, assumes one call at a time per pool. */
 hs_status hs_indexer_topk(hs_pool* pool, int32_t index_layer, int32_t n_tokens,
                           const int32_t* d_req, const int32_t* d_limit, const int8_t* d_q,
                           const int8_t* d_w, int32_t* d_topk, int64_t* d_scores,

@@ -889,8 +889,16 @@ hs_status launch_select(hs_pool* p, int n, const int64_t* scores, int ld, const 
                         int32_t* d_topk, cudaStream_t st, bool fp_keys, bool wide_ok, bool hist0_done) {
   const int G = select_wide_groups(p, n, wide_ok);
   if (G > 0) return launch_select_wide(p, n, scores, ld, d_limit, d_topk, fp_keys, G, hist0_done, st);
-  // many query tokens: one CTA per token, every token at once
-  if (wide_ok && n > num_sms() / 8) return launch_select_token(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
+  // Many query tokens, at most one per SM: every token's keys in chunks over the whole
+  // GPU (three launches, no cross-CTA waits), so the longest token no longer sets the
+  // time of the launch. More tokens than SMs: one CTA per token, which then keeps every
+  // SM busy. (Chunked measured faster at 128 tokens of 8K-241K keys, slower at 256
+  // tokens of ~80K keys.)
+  if (wide_ok && n > num_sms() / 8) {
+    if (n <= p->d.bsel_tokens && n <= num_sms())
+      return launch_select_batch(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
+    return launch_select_token(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
+  }
   // otherwise 16 CTAs per token: each CTA's chunk is smaller and every pass shorter
   return launch_select_cl<16>(p, n, scores, ld, d_limit, d_topk, fp_keys, st);
 }

@@ -57,6 +57,8 @@ struct Dev {
   float2* o_stats;      // [max_tokens, MAX_SPLITS, 64] per split and head: (max in log2 units, sum)
   uint8_t* sel_ws;      // [sel_ws_tokens] SelWs: wide top-K selection scratch, zero between launches
   int32_t sel_ws_tokens;
+  uint8_t* bsel;        // [bsel_tokens] BselTok: chunked selection scratch (many query tokens)
+  int32_t bsel_tokens;
 };
 
 enum Counter { C_RESIDENT = 0, C_HITS = 1, C_MISSES = 2, C_H2D = 3, C_D2H = 4, C_N = 8 };

@@ -360,6 +360,8 @@ hs_status hs_pool_init(const hs_pool_config* cfg, void* const* d_kv_layers, void
     if (tok > c.max_tokens) tok = c.max_tokens;
     D.sel_ws_tokens = tok;
     chk(dev_alloc(p, &D.sel_ws, (size_t)(tok > 0 ? tok : 1) * sizeof(SelWs), 0));
+    D.bsel_tokens = c.max_tokens < BS_MAX_TOKENS ? c.max_tokens : BS_MAX_TOKENS;
+    chk(dev_alloc(p, &D.bsel, (size_t)D.bsel_tokens * sizeof(BselTok), 0));
   }
   if (s == HS_OK) {
     if (cudaMemcpy(D.kv, d_kv_layers, sizeof(void*) * c.n_layers, cudaMemcpyHostToDevice) != cudaSuccess ||

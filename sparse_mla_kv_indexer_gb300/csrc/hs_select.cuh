@@ -123,4 +123,33 @@ hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, c
 hs_status launch_select_token(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
                               int32_t* d_topk, bool fp_keys, cudaStream_t st);
 
+// ---- chunked selection: many query tokens, every token's keys spread over the GPU ----
+constexpr int BS_CHUNK = 8192;                                  // keys per work item (16 per thread)
+constexpr int BS_CAND = 4096;                                   // most keys the threshold bucket may hold
+constexpr int BS_STAGE = 2048 + BS_CAND;                        // K (<= 2048) + BS_CAND staged keys
+constexpr int BS_MAX_CHUNKS = (HS_MAX_CTX + BS_CHUNK - 1) / BS_CHUNK;
+constexpr int BS_MAX_TOKENS = 8192;                             // query tokens per launch (shared-memory work list)
+
+// Per query token, in global memory. hist and done are zero between launches (the
+// last histogram CTA of a token resets done, the final kernel clears hist); the
+// other fields are written before they are read within a launch.
+struct BselTok {
+  uint32_t hist[SEL_BINS];              // level-0 histogram sums over the token's chunks
+  uint32_t done;                        // chunks whose histogram is in the sums
+  int32_t bin;                          // the threshold bucket: it holds the K-th largest key
+  int32_t need;                         // keys to take from it (K minus the keys in higher buckets)
+  int32_t crowded;                      // the bucket holds more than BS_CAND keys: full selection
+  uint32_t nstage;                      // keys staged so far (buckets >= bin)
+  int32_t pad[3];
+  uint32_t sbase[BS_MAX_CHUNKS];        // per chunk: its first staged key
+  uint32_t scount[BS_MAX_CHUNKS];       // per chunk: its staged keys, in ascending token order
+  unsigned long long stage[BS_STAGE];   // the keys in buckets >= bin, chunk by chunk
+};
+
+// Three launches: level-0 histograms (the last chunk of a token finds its threshold
+// bucket), staging of every key in that bucket or above, and per token tau and the
+// output from the staged keys.
+hs_status launch_select_batch(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                              int32_t* d_topk, bool fp_keys, cudaStream_t st);
+
 }  // namespace hs

@@ -1,4 +1,6 @@
-// Top-K selection spread over the whole GPU, for batches of few query tokens.
+// Top-K selection spread over the whole GPU: the wide selection for batches of few
+// query tokens (below), the chunked selection for many tokens up to one per SM, and
+// one CTA per token beyond that.
 //
 // "vLLM introduces Hybrid HiSparse hybrid sparse offloading for GLM 5.3" (vLLM
 // blog Part 1), section "Sparsity when you need it": each query token keeps the
@@ -543,6 +545,292 @@ select_wide_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int3
   }
 }
 
+
+// ---- chunked selection: many query tokens, each token's keys in chunks over the GPU ----
+// Token t with n_t > K keys owns BS_CHUNK-key chunks first[t] .. first[t + 1] - 1 of a
+// work list that every CTA builds in shared memory from the limits; a token with
+// n_t <= K owns none (the final kernel writes its output).
+constexpr int BS_THREADS = SW_THREADS;
+constexpr int BS_PER = 8;                              // keys per 16-byte-load step of a thread
+constexpr int BS_KPT = BS_CHUNK / BS_THREADS;          // keys per thread of a chunk
+static_assert(BS_KPT == 2 * BS_PER, "a chunk is two load steps of every thread");
+static_assert(HS_MAX_CTX % 2 == 0, "16-byte score loads stay inside a row");
+constexpr int BS_EPT = (BS_STAGE + BS_THREADS - 1) / BS_THREADS;   // staged keys per thread at the end
+constexpr int BS_FINAL_SMEM = BS_STAGE * 8 + 2 * (BS_MAX_CHUNKS + 1) * 4;
+
+__device__ __forceinline__ int bs_limit(const int32_t* limit_of, int tok, int max_ctx) {
+  const int n = limit_of[tok];
+  return max(0, min(n, max_ctx));
+}
+
+// first[0 .. n_tok] (shared memory): exclusive prefix of the tokens' chunk counts; returns the total.
+__device__ int bs_work_list(const int32_t* limit_of, int n_tok, int K, int max_ctx, int* first, int* warp_tot,
+                            int* s_total) {
+  int carry = 0;
+  for (int base = 0; base < n_tok; base += BS_THREADS) {
+    const int t = base + (int)threadIdx.x;
+    int c = 0;
+    if (t < n_tok) {
+      const int n = bs_limit(limit_of, t, max_ctx);
+      c = n > K ? (n + BS_CHUNK - 1) / BS_CHUNK : 0;
+    }
+    const int ex = block_excl_scan(c, warp_tot, s_total);
+    if (t < n_tok) first[t] = carry + ex;
+    carry += *s_total;
+  }
+  if (threadIdx.x == 0) first[n_tok] = carry;
+  __syncthreads();
+  return carry;
+}
+
+// the last t with first[t] <= w (the token that owns work item w)
+__device__ __forceinline__ int bs_token_of(const int* first, int n_tok, int w) {
+  int lo = 0, hi = n_tok;   // first[lo] <= w < first[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (first[mid] <= w) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Adds the CTA's histogram of nacc chunks of token B (of nch chunks) to the token's
+// sums and clears it; the CTA that completes the sums finds the threshold bucket.
+__device__ __noinline__ void bs_flush(BselTok* B, int nch, int nacc, int K, uint32_t* hist, int* warp_tot, int* s_bin,
+                                      long long* s_above, int* s_last) {
+  const int tid = threadIdx.x;
+  __syncthreads();
+  for (int b = tid; b < SEL_BINS; b += BS_THREADS) {
+    const uint32_t h = hist[b];
+    if (h) {
+      atomicAdd(&B->hist[b], h);
+      hist[b] = 0;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) *s_last = atomicAdd(&B->done, (uint32_t)nacc) + (uint32_t)nacc == (uint32_t)nch;
+  __syncthreads();
+  if (*s_last) {   // every chunk's histogram of this token is in the sums
+    __threadfence();
+    sw_find<true>(B->hist, K, warp_tot, s_bin, s_above);
+    if (tid == 0) {
+      B->bin = *s_bin;
+      B->need = K - (int)*s_above;
+      B->crowded = __ldcg(&B->hist[*s_bin]) > (uint32_t)BS_CAND;
+      B->nstage = 0;
+      B->done = 0;
+    }
+  }
+  __syncthreads();
+}
+
+// Pass 1: level-0 histograms. A CTA takes a contiguous run of chunks, sums the chunks
+// of one token in shared memory and adds them to the token's global sums when the
+// token changes; the CTA that completes a token's sums finds the bucket holding the
+// K-th largest key and whether it is crowded.
+__global__ void __launch_bounds__(BS_THREADS)
+bsel_hist_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of, int n_tok,
+                 int fp_keys) {
+  extern __shared__ __align__(16) int bs_first[];   // [n_tok + 1]
+  __shared__ __align__(16) uint32_t hist[SEL_BINS];
+  __shared__ int warp_tot[32];
+  __shared__ int s_total, s_bin, s_last;
+  __shared__ long long s_above;
+  const int tid = threadIdx.x, K = D.topk;
+  BselTok* T = reinterpret_cast<BselTok*>(D.bsel);
+  griddep_wait();
+  griddep_launch();
+  const int total = bs_work_list(limit_of, n_tok, K, D.max_ctx, bs_first, warp_tot, &s_total);
+  const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int w0 = min(total, (int)blockIdx.x * per), w1 = min(total, w0 + per);
+  for (int b = tid; b < SEL_BINS; b += BS_THREADS) hist[b] = 0;
+  __syncthreads();
+  int cur = -1, nacc = 0;
+  for (int w = w0; w < w1; ++w) {
+    const int tok = bs_token_of(bs_first, n_tok, w);
+    if (tok != cur) {
+      if (cur >= 0) bs_flush(T + cur, bs_first[cur + 1] - bs_first[cur], nacc, K, hist, warp_tot, &s_bin, &s_above, &s_last);
+      cur = tok;
+      nacc = 0;
+    }
+    const int c = w - bs_first[tok];
+    const int n = bs_limit(limit_of, tok, D.max_ctx);
+    const int lo = c * BS_CHUNK, hi = min(n, lo + BS_CHUNK);
+    const long long* s = reinterpret_cast<const long long*>(scores) + (size_t)tok * ld;
+    unsigned long long k[BS_PER];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lo + (2 * tid + h) * BS_PER;
+      const uint32_t v = st_load_lane<BS_PER>(s, i, hi, k, D.status);
+#pragma unroll
+      for (int j = 0; j < BS_PER; ++j)
+        if (v >> j & 1) atomicAdd(&hist[bucket_of(k[j], fp_keys != 0)], 1u);
+    }
+    ++nacc;
+  }
+  if (cur >= 0) bs_flush(T + cur, bs_first[cur + 1] - bs_first[cur], nacc, K, hist, warp_tot, &s_bin, &s_above, &s_last);
+}
+
+// Pass 2: each chunk stages its keys in the threshold bucket or above, in ascending
+// token order, at a range of its token's list that it reserves with one atomic.
+__global__ void __launch_bounds__(BS_THREADS)
+bsel_stage_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of, int n_tok,
+                  int fp_keys) {
+  extern __shared__ __align__(16) int bs_first[];
+  __shared__ int warp_tot[32];
+  __shared__ int s_total;
+  __shared__ uint32_t s_base;
+  const int tid = threadIdx.x, K = D.topk;
+  BselTok* T = reinterpret_cast<BselTok*>(D.bsel);
+  griddep_wait();
+  griddep_launch();
+  const int total = bs_work_list(limit_of, n_tok, K, D.max_ctx, bs_first, warp_tot, &s_total);
+  for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    const int tok = bs_token_of(bs_first, n_tok, w);
+    BselTok* B = T + tok;
+    if (__ldcg(&B->crowded)) continue;   // uniform: the final kernel selects this token in full
+    const int c = w - bs_first[tok];
+    const int n = bs_limit(limit_of, tok, D.max_ctx);
+    const int lo = c * BS_CHUNK, hi = min(n, lo + BS_CHUNK);
+    const long long* s = reinterpret_cast<const long long*>(scores) + (size_t)tok * ld;
+    const int bin = __ldcg(&B->bin);
+    unsigned long long k[BS_KPT];
+    uint32_t take = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lo + tid * BS_KPT + h * BS_PER;
+      unsigned long long kk[BS_PER];
+      const uint32_t v = st_load_lane<BS_PER>(s, i, hi, kk, D.status);
+#pragma unroll
+      for (int j = 0; j < BS_PER; ++j) {
+        k[h * BS_PER + j] = kk[j];
+        if ((v >> j & 1) && bucket_of(kk[j], fp_keys != 0) >= bin) take |= 1u << (h * BS_PER + j);
+      }
+    }
+    const int ex = block_excl_scan(__popc(take), warp_tot, &s_total);
+    if (tid == 0) {
+      s_base = atomicAdd(&B->nstage, (uint32_t)s_total);
+      B->sbase[c] = s_base;
+      B->scount[c] = (uint32_t)s_total;
+    }
+    __syncthreads();
+    uint32_t pos = s_base + (uint32_t)ex;
+#pragma unroll
+    for (int j = 0; j < BS_KPT; ++j)
+      if (take >> j & 1) {
+        if (pos < (uint32_t)BS_STAGE) B->stage[pos] = k[j];
+        else set_status(D.status, HS_ERR_BAD_ID);   // not reached: a bucket this full is crowded
+        ++pos;
+      }
+    __syncthreads();   // s_base, s_total
+  }
+}
+
+// Per token (one CTA, grid-stride over tokens): tau among the staged keys, then the
+// output: the staged keys >= tau in chunk order, which is ascending token order. A
+// token with at most K keys gets all of them (ascending, -1 after); a crowded one is
+// selected here in full. The token's sums are cleared for the next launch.
+__global__ void __launch_bounds__(BS_THREADS)
+bsel_final_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32_t* __restrict__ limit_of,
+                  int32_t* __restrict__ topk, int n_tok, int fp_keys) {
+  extern __shared__ __align__(16) unsigned long long bs_dyn[];
+  unsigned long long* st = bs_dyn;                                  // [BS_STAGE] staged keys
+  int* s_pre = reinterpret_cast<int*>(st + BS_STAGE);                // [BS_MAX_CHUNKS + 1] chunk-order prefix
+  int* s_sb = s_pre + BS_MAX_CHUNKS + 1;                             // [BS_MAX_CHUNKS] chunk's first staged key
+  __shared__ __align__(16) uint32_t hist[SEL_BINS];
+  __shared__ int warp_tot[32];
+  __shared__ __align__(16) int s_small[2 + 2 * (SW_THREADS / 32) + 2 + 4];
+  __shared__ int s_bin, s_total;
+  __shared__ long long s_above;
+  __shared__ unsigned long long s_tau;
+  static_assert(BS_STAGE >= SW_CAND, "the staged-key buffer serves the full selection's candidates");
+  const int tid = threadIdx.x, K = D.topk;
+  BselTok* T = reinterpret_cast<BselTok*>(D.bsel);
+  griddep_wait();
+  griddep_launch();
+  for (int tok = blockIdx.x; tok < n_tok; tok += gridDim.x) {
+    const int n = bs_limit(limit_of, tok, D.max_ctx);
+    int32_t* out = topk + (size_t)tok * K;
+    if (n <= K) {
+      for (int i = tid; i < K; i += BS_THREADS) out[i] = i < n ? i : -1;
+      continue;   // uniform: no chunks, no sums
+    }
+    BselTok* B = T + tok;
+    if (__ldcg(&B->crowded)) {   // the threshold bucket is crowded: the full selection
+      select_token_cta<8>(reinterpret_cast<const long long*>(scores) + (size_t)tok * ld, n, K, fp_keys != 0, out,
+                          D.status, hist, st, warp_tot, s_small);
+    } else {
+      const int m = min((int)__ldcg(&B->nstage), BS_STAGE), nch = (n + BS_CHUNK - 1) / BS_CHUNK;
+      for (int i = tid; i < m; i += BS_THREADS) st[i] = __ldcg(&B->stage[i]);
+      for (int x = tid; x < nch; x += BS_THREADS) {
+        s_sb[x] = (int)__ldcg(&B->sbase[x]);
+        s_pre[x + 1] = (int)__ldcg(&B->scount[x]);
+      }
+      __syncthreads();
+      if (tid == 0) {   // at most BS_MAX_CHUNKS additions in shared memory
+        s_pre[0] = 0;
+        for (int x = 1; x <= nch; ++x) s_pre[x] += s_pre[x - 1];
+      }
+      unsigned long long base, width;
+      bucket_range(__ldcg(&B->bin), fp_keys != 0, base, width);
+      int lcnt = m, lneed = __ldcg(&B->need);
+      __syncthreads();
+      while (lcnt > 1 && width > 1) {   // narrow the bucket's range to the single key tau
+        const int shift = refine_shift(width);
+        for (int b = tid; b < SEL_BINS; b += BS_THREADS) hist[b] = 0;
+        __syncthreads();
+        for (int i = tid; i < m; i += BS_THREADS)
+          if (in_range(st[i], base, width)) atomicAdd(&hist[(int)((st[i] - base) >> shift)], 1u);
+        __syncthreads();
+        sw_find<false>(hist, lneed, warp_tot, &s_bin, &s_above);
+        lcnt = (int)hist[s_bin];
+        base += (unsigned long long)s_bin << shift;
+        lneed -= (int)s_above;
+        width = 1ull << shift;
+        __syncthreads();
+      }
+      if (tid == 0) s_tau = base;
+      __syncthreads();
+      if (width > 1)
+        for (int i = tid; i < m; i += BS_THREADS)
+          if (in_range(st[i], base, width)) s_tau = st[i];
+      __syncthreads();
+      const unsigned long long tau = s_tau;
+      // virtual position v = s_pre[c] + (e - s_sb[c]) orders the staged keys by chunk
+      const int mv = s_pre[nch];
+      unsigned long long kv[BS_EPT];
+      int cnt = 0;
+#pragma unroll
+      for (int j = 0; j < BS_EPT; ++j) {
+        const int v = tid * BS_EPT + j;
+        kv[j] = 0;
+        if (v < mv) {
+          int lo = 0, hi = nch;   // s_pre[lo] <= v < s_pre[hi]
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_pre[mid] <= v) lo = mid;
+            else hi = mid;
+          }
+          const int e = s_sb[lo] + (v - s_pre[lo]);
+          if (e < m) kv[j] = st[e];
+        }
+        cnt += kv[j] >= tau && v < mv;
+      }
+      int pos = block_excl_scan(cnt, warp_tot, &s_total);
+#pragma unroll
+      for (int j = 0; j < BS_EPT; ++j)
+        if (tid * BS_EPT + j < mv && kv[j] >= tau) {
+          if (pos < K) out[pos] = sel_token(kv[j]);
+          ++pos;
+        }
+      if (tid == 0 && s_total != K) set_status(D.status, HS_ERR_BAD_ID);   // exactly K keys are >= tau
+    }
+    for (int b = tid; b < SEL_BINS; b += BS_THREADS) B->hist[b] = 0;
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 hs_status launch_select_token(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
@@ -551,6 +839,26 @@ hs_status launch_select_token(hs_pool* p, int n, const int64_t* scores, int ld, 
   const int grid = n < num_sms() ? n : num_sms();
   return launch_pdl(select_token_kernel, dim3(grid), dim3(SW_THREADS), 0, st, 0, p->d, scores, ld, d_limit, d_topk,
                     n, fp_keys ? 1 : 0);
+}
+
+hs_status launch_select_batch(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
+                              int32_t* d_topk, bool fp_keys, cudaStream_t st) {
+  if (n < 1 || n > p->d.bsel_tokens || !p->d.bsel) return HS_ERR_INVALID;
+  const int smem = (n + 1) * (int)sizeof(int);
+  constexpr int smem_max = (BS_MAX_TOKENS + 1) * (int)sizeof(int);
+  if (ensure_kernel_attrs(bsel_hist_kernel, smem_max) != HS_OK || ensure_kernel_attrs(bsel_stage_kernel, smem_max) != HS_OK ||
+      ensure_kernel_attrs(bsel_final_kernel, BS_FINAL_SMEM) != HS_OK)
+    return HS_ERR_CUDA;
+  const int grid = 2 * num_sms(), fk = fp_keys ? 1 : 0;
+  hs_status s = launch_pdl(bsel_hist_kernel, dim3(grid), dim3(BS_THREADS), smem, st, 0, p->d, scores, ld, d_limit, n, fk);
+  if (s == HS_OK)
+    s = launch_pdl(bsel_stage_kernel, dim3(grid), dim3(BS_THREADS), smem, st, 0, p->d, scores, ld, d_limit, n, fk);
+  if (s == HS_OK)
+    s = launch_pdl(bsel_final_kernel, dim3(n < 2 * num_sms() ? n : 2 * num_sms()), dim3(BS_THREADS), BS_FINAL_SMEM, st,
+                   0, p->d, scores, ld, d_limit, d_topk, n, fk);
+  if (s != HS_OK)   // a launch after the first failed: its sums must not reach the next call
+    cudaMemsetAsync(p->d.bsel, 0, (size_t)p->d.bsel_tokens * sizeof(BselTok), st);
+  return s;
 }
 
 hs_status launch_select_wide(hs_pool* p, int n, const int64_t* scores, int ld, const int32_t* d_limit,
