@@ -695,19 +695,17 @@ bsel_stage_kernel(Dev D, const int64_t* __restrict__ scores, int ld, const int32
     const int lo = c * BS_CHUNK, hi = min(n, lo + BS_CHUNK);
     const long long* s = reinterpret_cast<const long long*>(scores) + (size_t)tok * ld;
     const int bin = __ldcg(&B->bin);
-    unsigned long long k[BS_KPT];
+    unsigned long long k[BS_KPT], k1[BS_PER];
+    // both halves' loads first, then the buckets
+    const uint32_t v0 = st_load_lane<BS_PER>(s, lo + tid * BS_KPT, hi, *reinterpret_cast<unsigned long long(*)[BS_PER]>(k), D.status);
+    const uint32_t v1 = st_load_lane<BS_PER>(s, lo + tid * BS_KPT + BS_PER, hi, k1, D.status);
+#pragma unroll
+    for (int j = 0; j < BS_PER; ++j) k[BS_PER + j] = k1[j];
+    const uint32_t valid = v0 | (v1 << BS_PER);
     uint32_t take = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = lo + tid * BS_KPT + h * BS_PER;
-      unsigned long long kk[BS_PER];
-      const uint32_t v = st_load_lane<BS_PER>(s, i, hi, kk, D.status);
-#pragma unroll
-      for (int j = 0; j < BS_PER; ++j) {
-        k[h * BS_PER + j] = kk[j];
-        if ((v >> j & 1) && bucket_of(kk[j], fp_keys != 0) >= bin) take |= 1u << (h * BS_PER + j);
-      }
-    }
+    for (int j = 0; j < BS_KPT; ++j)
+      if ((valid >> j & 1) && bucket_of(k[j], fp_keys != 0) >= bin) take |= 1u << j;
     const int ex = block_excl_scan(__popc(take), warp_tot, &s_total);
     if (tid == 0) {
       s_base = atomicAdd(&B->nstage, (uint32_t)s_total);
@@ -849,8 +847,11 @@ hs_status launch_select_batch(hs_pool* p, int n, const int64_t* scores, int ld, 
   if (ensure_kernel_attrs(bsel_hist_kernel, smem_max) != HS_OK || ensure_kernel_attrs(bsel_stage_kernel, smem_max) != HS_OK ||
       ensure_kernel_attrs(bsel_final_kernel, BS_FINAL_SMEM) != HS_OK)
     return HS_ERR_CUDA;
+  // two CTAs per SM for the staging pass (its registers), three for the lighter
+  // histogram pass: more chunks in flight per SM
   const int grid = 2 * num_sms(), fk = fp_keys ? 1 : 0;
-  hs_status s = launch_pdl(bsel_hist_kernel, dim3(grid), dim3(BS_THREADS), smem, st, 0, p->d, scores, ld, d_limit, n, fk);
+  hs_status s = launch_pdl(bsel_hist_kernel, dim3(3 * num_sms()), dim3(BS_THREADS), smem, st, 0, p->d, scores, ld,
+                           d_limit, n, fk);
   if (s == HS_OK)
     s = launch_pdl(bsel_stage_kernel, dim3(grid), dim3(BS_THREADS), smem, st, 0, p->d, scores, ld, d_limit, n, fk);
   if (s == HS_OK)
