@@ -59,11 +59,12 @@
 extern "C" {
 #endif
 
-/* Longest context a pool accepts (tokens per request). With many query tokens the
- * top-K selection splits a token's scores over a 16-CTA cluster and keeps a 2-byte
- * bucket per score of its share in shared memory, which bounds the share at 81,920
- * scores. (With few query tokens the selection spreads each token over up to one CTA
- * per SM, holding at most 12,288 scores per CTA.) */
+/* Longest context a pool accepts (tokens per request). The cluster top-K selection
+ * (a middling number of query tokens, and hs_indexer_topk_noalloc) splits a token's
+ * scores over a 16-CTA cluster and keeps a 2-byte bucket per score of its share in
+ * shared memory, which bounds the share at 81,920 scores. (With few query tokens the
+ * selection spreads each token over up to one CTA per SM, holding at most 12,288 scores
+ * per CTA; with many it cuts each token into chunks of 8,192 scores.) */
 #define HS_MAX_CTX 1310720
 
 typedef struct CUstream_st* hs_stream_t; /* a cudaStream_t; NULL = legacy default stream */
